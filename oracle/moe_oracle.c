@@ -1,0 +1,370 @@
+/*
+ * CPU oracle for the weight-only 4-bit fused Mixture-of-Experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this file: it is used by tests/, by the smoke check and by the timed
+ * CPU baseline of the benchmark.  It shares no code, header, table or helper
+ * with the CUDA library.
+ *
+ * What it computes (plain definitions, written out, fp64 accumulation):
+ *
+ *   decode      the 4-bit codes and scale bytes from their bit-level definitions
+ *               (uint4b8 of "Marlin MoE kernel occupancy ..." (sglang PR #31552),
+ *               test_fused_marlin_moe_large_non_ep_schedule: quant_type uint4b8;
+ *               E2M1 / E8M0 / E4M3 from the OCP microscaling and FP8 formats, which
+ *               the pages name but do not define);
+ *   dequant     W = (q-8)*s (int4, group along the reduction dim),
+ *               W = e2m1*2^(b-127) (MXFP4, one E8M0 byte per 32),
+ *               W = e2m1*e4m3*gs[e] (NVFP4, one E4M3 per 16, one fp32 global
+ *               scale per expert shared by gate and up: "013-moe-middle-tiles.py",
+ *               Weights and _marlin_layer);
+ *   deinterleave  GPT-OSS w13 rows [g0,u0,g1,u1,...] -> gate i = row 2i, up i = row
+ *               2i+1 ("SM120 MXFP4 MoE ... Marlin" (sglang PR #28231),
+ *               deinterleave_moe_mxfp4_w13_for_marlin);
+ *   align       sort the local (token, slot) pairs by expert and pad each expert's
+ *               run to block_m ("013-moe-middle-tiles.py", kernel_fn:
+ *               moe_align_block_size(local_ids, block_size_m, ...));
+ *   FFN         per local pair p=(t,j) with expert e:
+ *                 h = bf16(gs13 * sum_k x[t,k] W13[e,r,k] + b13[e,r])       r < 2N
+ *                 a = bf16(act(h[n], h[N+n]))   gate = first half, up = second
+ *                 y = bf16(gs2 * sum_n a[n] W2[e,c,n] + b2[e,c])            c < K
+ *               act = silu(g)*u (silu_and_mul) or
+ *                     g' = min(g, L), u' = clamp(u,-L,L), g'*sigmoid(alpha*g')*(u'+1)
+ *               (swiglu_gpt_oss_sigmoid_alpha_contiguous of PR #28231);
+ *   combine     out[t] = bf16(rsf * sum_j w[t,j] * y[t,j]) over local slots
+ *               (the per-expert reference loop of the PR #31552 test), or with the
+ *               post-expert norm of "013-moe-middle-tiles.py" (_expert_norm_factors,
+ *               _expert_norm_sum, weight_first):
+ *                 z = y * nw,  nw = bf16(fp32(1 + w_norm)),
+ *                 inv = 1 / sqrt(sum_c z^2 / K + eps),
+ *                 out[t] = bf16(rsf * sum_j w[t,j] * inv_j * z_j).
+ *
+ * The three bf16 roundings of the FFN (after GEMM1+bias, after the activation,
+ * after GEMM2+bias) are where the pages' own pipeline stores bf16 intermediates
+ * (cache1 / cache2 / cache3 of kernel_fn).  Non-local pairs contribute nothing.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_INT4 = 0, ORC_MXFP4 = 1, ORC_NVFP4 = 2 };
+enum { ORC_SILU_MUL = 0, ORC_SIGMOID_ALPHA = 1 };
+
+/* ------------------------------------------------------------------ formats */
+
+/* bf16 is the high half of an IEEE binary32. */
+double orc_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 (8 significant bits, ties to even),
+ * keeping bf16 subnormals (quantum 2^-133) and overflowing to infinity. */
+uint16_t orc_bf16_round(double x) {
+    if (isnan(x)) return 0x7FC0;
+    int neg = signbit(x) != 0;
+    double a = fabs(x);
+    if (a == 0.0) return neg ? 0x8000 : 0x0000;
+    int ex;
+    frexp(a, &ex);            /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;           /* a in [2^e, 2^(e+1)) */
+    double quantum = (e < -126) ? ldexp(1.0, -133) : ldexp(1.0, e - 7);
+    double r = nearbyint(a / quantum) * quantum;  /* default mode: ties to even */
+    float f;
+    if (r > 3.3895313892515355e38) {              /* largest finite bf16 */
+        f = INFINITY;
+    } else {
+        f = (float)r;                               /* exact: r has <= 8 bits */
+    }
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t b = (uint16_t)(u >> 16);
+    return neg ? (uint16_t)(b | 0x8000) : b;
+}
+
+/* E2M1: sign | 2-bit exponent (bias 1) | 1-bit mantissa; exponent 0 is subnormal. */
+double orc_e2m1_value(unsigned code) {
+    unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+    double mag = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, (int)e - 1);
+    return s ? -mag : mag;
+}
+
+/* E8M0: a bare biased exponent, 2^(b-127); 0xFF is NaN. */
+double orc_e8m0_value(unsigned b) {
+    b &= 0xFFu;
+    if (b == 0xFFu) return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* E4M3 (fn variant): sign | 4-bit exponent (bias 7) | 3-bit mantissa,
+ * subnormals m/8 * 2^-6, S.1111.111 is NaN, no infinities. */
+double orc_e4m3_value(unsigned b) {
+    b &= 0xFFu;
+    unsigned s = b >> 7, e = (b >> 3) & 15u, m = b & 7u;
+    if (e == 15u && m == 7u) return NAN;
+    double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    return s ? -mag : mag;
+}
+
+/* uint4b8: a 4-bit unsigned code q standing for q - 8. */
+double orc_int4_value(unsigned q) { return (double)((int)(q & 15u) - 8); }
+
+/* Element c of a packed row: byte c/2, low nibble for even c, high for odd. */
+static unsigned nibble(const uint8_t* row, long c) {
+    uint8_t b = row[c >> 1];
+    return (c & 1) ? (unsigned)(b >> 4) : (unsigned)(b & 15u);
+}
+
+static double code_value(int fmt, unsigned q) {
+    return fmt == ORC_INT4 ? orc_int4_value(q) : orc_e2m1_value(q);
+}
+
+/* Scale value of entry idx of a scale array in format fmt. */
+static double scale_value(int fmt, const void* scales, long idx) {
+    if (fmt == ORC_INT4) return orc_bf16_value(((const uint16_t*)scales)[idx]);
+    if (fmt == ORC_MXFP4) return orc_e8m0_value(((const uint8_t*)scales)[idx]);
+    return orc_e4m3_value(((const uint8_t*)scales)[idx]);
+}
+
+static int scale_bytes(int fmt) { return fmt == ORC_INT4 ? 2 : 1; }
+
+/*
+ * Dequantise logical rows [0, rows) of one expert's matrix, cols along the
+ * reduction dimension, into out[rows][cols] (without the NVFP4 global scale,
+ * which the caller applies to the fp64 sum).  row_map[r] gives the stored row
+ * of logical row r (identity when NULL); it is how interleaved gate/up rows are
+ * read.  Every product q*s is exact in binary32 for the three formats.
+ */
+void orc_dequant(int fmt, const uint8_t* codes, const void* scales, int rows, int cols, int group,
+                 const int32_t* row_map, float* out) {
+    long bpr = cols / 2, spr = cols / group;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        long sr = row_map ? row_map[r] : r;
+        const uint8_t* crow = codes + sr * bpr;
+        for (long c = 0; c < cols; ++c) {
+            double v = code_value(fmt, nibble(crow, c)) * scale_value(fmt, scales, sr * spr + c / group);
+            out[(long)r * cols + c] = (float)v;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ align */
+
+/* Worst-case number of sorted slots: every non-empty expert wastes at most
+ * block_m - 1 slots, and at most min(E, M*k) experts are non-empty. */
+long orc_align_capacity(int M, int top_k, int num_experts, int block_m) {
+    long pairs = (long)M * top_k;
+    long busy = pairs < num_experts ? pairs : num_experts;
+    long n = pairs + busy * (block_m - 1);
+    return (n + block_m - 1) / block_m * block_m;
+}
+
+/*
+ * Align the local pairs to block_m.  A pair is the flat index p = t*k + j; its
+ * routed id topk_ids[p] is local when base <= id < base + E.
+ *   - experts appear in ascending local id, empty experts get no block;
+ *   - within an expert the pairs are in ascending p;
+ *   - each expert's run is padded to a multiple of block_m with the sentinel M*k;
+ *   - n_padded = sum_e ceil(count_e / block_m) * block_m;
+ *   - sorted_ids[n_padded, cap) = sentinel, expert_ids[b] = expert of block b,
+ *     -1 for blocks at or past n_padded / block_m.
+ * Returns 0, or -1 on bad arguments.
+ */
+int orc_align(const int32_t* topk_ids, int M, int top_k, int base, int num_experts, int block_m,
+              int32_t* sorted_ids, long cap, int32_t* expert_ids, int32_t* n_padded) {
+    if (M < 0 || top_k <= 0 || num_experts <= 0 || block_m <= 0) return -1;
+    long pairs = (long)M * top_k;
+    int32_t sentinel = (int32_t)pairs;
+    long* count = (long*)calloc((size_t)num_experts, sizeof(long));
+    long* start = (long*)calloc((size_t)num_experts, sizeof(long));
+    if (!count || !start) { free(count); free(start); return -1; }
+    for (long p = 0; p < pairs; ++p) {
+        long e = (long)topk_ids[p] - base;
+        if (e >= 0 && e < num_experts) count[e]++;
+    }
+    long total = 0;
+    for (int e = 0; e < num_experts; ++e) {
+        start[e] = total;
+        total += (count[e] + block_m - 1) / block_m * block_m;
+    }
+    if (total > cap) { free(count); free(start); return -1; }
+    for (long i = 0; i < cap; ++i) sorted_ids[i] = sentinel;
+    for (long b = 0; b < cap / block_m; ++b) expert_ids[b] = -1;
+    long* fill = (long*)calloc((size_t)num_experts, sizeof(long));
+    for (long p = 0; p < pairs; ++p) {
+        long e = (long)topk_ids[p] - base;
+        if (e >= 0 && e < num_experts) sorted_ids[start[e] + fill[e]++] = (int32_t)p;
+    }
+    for (int e = 0; e < num_experts; ++e)
+        for (long b = start[e] / block_m; b < (start[e] + (count[e] + block_m - 1) / block_m * block_m) / block_m; ++b)
+            expert_ids[b] = e;
+    *n_padded = (int32_t)total;
+    free(count); free(start); free(fill);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ forward */
+
+typedef struct {
+    int fmt, num_experts, hidden, inter, group, interleaved;
+    const uint8_t* w13;   /* [E, 2N, K/2] */
+    const void* w13_s;    /* [E, 2N, K/g] */
+    const float* w13_gs;  /* [E] or NULL */
+    const uint16_t* b13;  /* [E, 2N] bf16 or NULL */
+    const uint8_t* w2;    /* [E, K, N/2] */
+    const void* w2_s;     /* [E, K, N/g] */
+    const float* w2_gs;   /* [E] or NULL */
+    const uint16_t* b2;   /* [E, K] bf16 or NULL */
+} orc_layer;
+
+typedef struct {
+    int M, top_k, expert_base, act;
+    double alpha, limit, rsf, norm_eps;
+    const uint16_t* x;            /* [M, K] bf16 */
+    const int32_t* topk_ids;      /* [M, k] */
+    const float* topk_weights;    /* [M, k] */
+    const uint16_t* post_norm_w;  /* [K] bf16 raw w (applied as 1 + w) or NULL */
+} orc_batch;
+
+static double round_bf16(double v) { return orc_bf16_value(orc_bf16_round(v)); }
+
+static double activation(int act, double g, double u, double alpha, double limit) {
+    if (act == ORC_SILU_MUL) return g / (1.0 + exp(-g)) * u;
+    double gc = g < limit ? g : limit;
+    double uc = u > limit ? limit : (u < -limit ? -limit : u);
+    return gc * (1.0 / (1.0 + exp(-alpha * gc))) * (uc + 1.0);
+}
+
+/* y[K] of one pair whose expert weights are already dequantised. */
+static void ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, const float* W13,
+                     const float* W2, double* h, double* a, double* y) {
+    const int K = L->hidden, N = L->inter;
+    const uint16_t* xr = X->x + (long)t * K;
+    double gs13 = L->w13_gs ? (double)L->w13_gs[e] : 1.0;
+    double gs2 = L->w2_gs ? (double)L->w2_gs[e] : 1.0;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < 2 * N; ++r) {
+        const float* wr = W13 + (long)r * K;
+        double acc = 0.0;
+        for (int c = 0; c < K; ++c) acc += orc_bf16_value(xr[c]) * (double)wr[c];
+        long br = L->interleaved ? (long)2 * (r % N) + (r / N) : r;
+        double b = L->b13 ? orc_bf16_value(L->b13[(long)e * 2 * N + br]) : 0.0;
+        h[r] = round_bf16(gs13 * acc + b);
+    }
+    for (int n = 0; n < N; ++n)
+        a[n] = round_bf16(activation(X->act, h[n], h[N + n], X->alpha, X->limit));
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < K; ++c) {
+        const float* wr = W2 + (long)c * N;
+        double acc = 0.0;
+        for (int n = 0; n < N; ++n) acc += a[n] * (double)wr[n];
+        double b = L->b2 ? orc_bf16_value(L->b2[(long)e * K + c]) : 0.0;
+        y[c] = round_bf16(gs2 * acc + b);
+    }
+}
+
+/*
+ * Output rows of the tokens listed in tokens[0, n_tokens) (each 0 <= t < M):
+ * out_bf16[i][K] gets token tokens[i]; out_acc (optional, [n_tokens][K]) gets the
+ * same value before its final bf16 rounding.  Only experts touched by those
+ * tokens are dequantised, one at a time.  Returns 0, or -1 on bad arguments or
+ * allocation failure.
+ */
+int orc_forward(const orc_layer* L, const orc_batch* X, const int32_t* tokens, int n_tokens,
+                uint16_t* out_bf16, double* out_acc) {
+    const int K = L->hidden, N = L->inter, E = L->num_experts, k = X->top_k;
+    if (K <= 0 || N <= 0 || E <= 0 || k <= 0 || L->group <= 0) return -1;
+    if (K % L->group || N % L->group || K % 2 || N % 2) return -1;
+    double* acc_out = (double*)calloc((size_t)n_tokens * K, sizeof(double));
+    double* nsq = (double*)calloc((size_t)n_tokens * k, sizeof(double));
+    float* W13 = (float*)malloc(sizeof(float) * (size_t)2 * N * K);
+    float* W2 = (float*)malloc(sizeof(float) * (size_t)K * N);
+    int32_t* rmap = (int32_t*)malloc(sizeof(int32_t) * 2 * (size_t)N);
+    double* h = (double*)malloc(sizeof(double) * 2 * (size_t)N);
+    double* a = (double*)malloc(sizeof(double) * (size_t)N);
+    double* y = (double*)malloc(sizeof(double) * (size_t)K);
+    double* nw = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!acc_out || !nsq || !W13 || !W2 || !rmap || !h || !a || !y || !nw) {
+        free(acc_out); free(nsq); free(W13); free(W2); free(rmap); free(h); free(a); free(y); free(nw);
+        return -1;
+    }
+    for (int r = 0; r < 2 * N; ++r)  /* logical row r -> stored row */
+        rmap[r] = L->interleaved ? 2 * (r % N) + (r / N) : r;
+    if (X->post_norm_w)
+        for (int c = 0; c < K; ++c) {
+            float s = (float)(1.0 + orc_bf16_value(X->post_norm_w[c]));  /* fp32 add, as torch */
+            nw[c] = round_bf16((double)s);
+        }
+    const long sb = scale_bytes(L->fmt);
+    for (int e = 0; e < E; ++e) {
+        int touched = 0;
+        for (int i = 0; i < n_tokens && !touched; ++i)
+            for (int j = 0; j < k; ++j)
+                if (X->topk_ids[(long)tokens[i] * k + j] - X->expert_base == e) { touched = 1; break; }
+        if (!touched) continue;
+        orc_dequant(L->fmt, L->w13 + (long)e * 2 * N * (K / 2),
+                    (const uint8_t*)L->w13_s + (long)e * 2 * N * (K / L->group) * sb, 2 * N, K, L->group,
+                    rmap, W13);
+        orc_dequant(L->fmt, L->w2 + (long)e * K * (N / 2),
+                    (const uint8_t*)L->w2_s + (long)e * K * (N / L->group) * sb, K, N, L->group, NULL, W2);
+        for (int i = 0; i < n_tokens; ++i) {
+            int t = tokens[i];
+            for (int j = 0; j < k; ++j) {
+                if (X->topk_ids[(long)t * k + j] - X->expert_base != e) continue;
+                ffn_pair(L, X, e, t, W13, W2, h, a, y);
+                double w = (double)X->topk_weights[(long)t * k + j];
+                double* acc = acc_out + (long)i * K;
+                if (X->post_norm_w) {
+                    double ss = 0.0;
+                    for (int c = 0; c < K; ++c) { double z = y[c] * nw[c]; ss += z * z; }
+                    double inv = 1.0 / sqrt(ss / K + X->norm_eps);
+                    for (int c = 0; c < K; ++c) acc[c] += w * inv * (y[c] * nw[c]);
+                } else {
+                    for (int c = 0; c < K; ++c) acc[c] += w * y[c];
+                }
+            }
+        }
+    }
+    for (long i = 0; i < (long)n_tokens * K; ++i) {
+        double v = X->rsf * acc_out[i];
+        if (out_acc) out_acc[i] = v;
+        if (out_bf16) out_bf16[i] = orc_bf16_round(v);
+    }
+    free(acc_out); free(nsq); free(W13); free(W2); free(rmap); free(h); free(a); free(y); free(nw);
+    return 0;
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Intermediates of one pair (token t on local expert e): h[2N], a[N], y[K]
+ * as the bf16-rounded values the forward uses.  Returns 0 or -1. */
+int orc_ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, double* h, double* a, double* y) {
+    const int K = L->hidden, N = L->inter;
+    if (e < 0 || e >= L->num_experts || t < 0 || t >= X->M) return -1;
+    float* W13 = (float*)malloc(sizeof(float) * (size_t)2 * N * K);
+    float* W2 = (float*)malloc(sizeof(float) * (size_t)K * N);
+    int32_t* rmap = (int32_t*)malloc(sizeof(int32_t) * 2 * (size_t)N);
+    if (!W13 || !W2 || !rmap) { free(W13); free(W2); free(rmap); return -1; }
+    for (int r = 0; r < 2 * N; ++r) rmap[r] = L->interleaved ? 2 * (r % N) + (r / N) : r;
+    const long sb = scale_bytes(L->fmt);
+    orc_dequant(L->fmt, L->w13 + (long)e * 2 * N * (K / 2),
+                (const uint8_t*)L->w13_s + (long)e * 2 * N * (K / L->group) * sb, 2 * N, K, L->group, rmap, W13);
+    orc_dequant(L->fmt, L->w2 + (long)e * K * (N / 2),
+                (const uint8_t*)L->w2_s + (long)e * K * (N / L->group) * sb, K, N, L->group, NULL, W2);
+    ffn_pair(L, X, e, t, W13, W2, h, a, y);
+    free(W13); free(W2); free(rmap);
+    return 0;
+}
