@@ -200,7 +200,7 @@ def forward(weights, batch, *, expert_base: int = 0, act: str = "silu_mul", alph
 
 def ffn_pair(weights, batch, e: int, t: int, *, expert_base: int = 0, act: str = "silu_mul",
              alpha: float = 1.702, limit: float = float("inf")):
-    """(h[2N], a[N], y[K]) of token t on local expert e, as bf16-rounded fp64."""
+    """(h[2N], a[N], y[K]) of token t on local expert e, in fp64."""
     keep = []
     layer, b = _structs(weights, batch, expert_base, act, alpha, limit, 1.0, 1e-8, False, keep)
     N, K = weights.N, weights.K

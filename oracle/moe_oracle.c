@@ -25,9 +25,9 @@
  *               run to block_m ("013-moe-middle-tiles.py", kernel_fn:
  *               moe_align_block_size(local_ids, block_size_m, ...));
  *   FFN         per local pair p=(t,j) with expert e:
- *                 h = bf16(gs13 * sum_k x[t,k] W13[e,r,k] + b13[e,r])       r < 2N
- *                 a = bf16(act(h[n], h[N+n]))   gate = first half, up = second
- *                 y = bf16(gs2 * sum_n a[n] W2[e,c,n] + b2[e,c])            c < K
+ *                 h = gs13 * sum_k x[t,k] W13[e,r,k] + b13[e,r]       r < 2N
+ *                 a = act(h[n], h[N+n])     gate = first half, up = second
+ *                 y = gs2 * sum_n a[n] W2[e,c,n] + b2[e,c]            c < K
  *               act = silu(g)*u (silu_and_mul) or
  *                     g' = min(g, L), u' = clamp(u,-L,L), g'*sigmoid(alpha*g')*(u'+1)
  *               (swiglu_gpt_oss_sigmoid_alpha_contiguous of PR #28231);
@@ -39,9 +39,11 @@
  *                 inv = 1 / sqrt(sum_c z^2 / K + eps),
  *                 out[t] = bf16(rsf * sum_j w[t,j] * inv_j * z_j).
  *
- * The three bf16 roundings of the FFN (after GEMM1+bias, after the activation,
- * after GEMM2+bias) are where the pages' own pipeline stores bf16 intermediates
- * (cache1 / cache2 / cache3 of kernel_fn).  Non-local pairs contribute nothing.
+ * h, a and y are carried exactly (fp64); the only rounding is the bf16 output.
+ * The bf16 intermediates of kernel_fn (cache1 / cache2 / cache3) are that
+ * implementation's storage, not part of the layer's definition, which is the
+ * per-expert matmul chain combined in fp32 of the PR #31552 reference loop.
+ * Non-local pairs contribute nothing.
  */
 #include <math.h>
 #include <stdint.h>
@@ -256,17 +258,17 @@ static void ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, const
         for (int c = 0; c < K; ++c) acc += orc_bf16_value(xr[c]) * (double)wr[c];
         long br = L->interleaved ? (long)2 * (r % N) + (r / N) : r;
         double b = L->b13 ? orc_bf16_value(L->b13[(long)e * 2 * N + br]) : 0.0;
-        h[r] = round_bf16(gs13 * acc + b);
+        h[r] = gs13 * acc + b;
     }
     for (int n = 0; n < N; ++n)
-        a[n] = round_bf16(activation(X->act, h[n], h[N + n], X->alpha, X->limit));
+        a[n] = activation(X->act, h[n], h[N + n], X->alpha, X->limit);
 #pragma omp parallel for schedule(static)
     for (int c = 0; c < K; ++c) {
         const float* wr = W2 + (long)c * N;
         double acc = 0.0;
         for (int n = 0; n < N; ++n) acc += a[n] * (double)wr[n];
         double b = L->b2 ? orc_bf16_value(L->b2[(long)e * K + c]) : 0.0;
-        y[c] = round_bf16(gs2 * acc + b);
+        y[c] = gs2 * acc + b;
     }
 }
 
@@ -350,7 +352,7 @@ int orc_num_threads(void) {
 }
 
 /* Intermediates of one pair (token t on local expert e): h[2N], a[N], y[K]
- * as the bf16-rounded values the forward uses.  Returns 0 or -1. */
+ * as the forward computes them.  Returns 0 or -1. */
 int orc_ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, double* h, double* a, double* y) {
     const int K = L->hidden, N = L->inter;
     if (e < 0 || e >= L->num_experts || t < 0 || t >= X->M) return -1;

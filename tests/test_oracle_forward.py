@@ -67,8 +67,8 @@ def decode_matrix(fmt, codes, scales, group):
 
 
 def dense_reference(wl, W, X, rsf=1.0):
-    """Every expert on every token, then select; fp64 sums, bf16 at the three
-    stored intermediates, bf16 output."""
+    """Every expert on every token, then select; fp64 throughout, the caller
+    rounds the output to bf16."""
     E, K, N = W.E, W.K, W.N
     W13 = decode_matrix(W.fmt, W.w13, W.w13_s, W.group)  # [E, 2N, K]
     b13 = bf16v(W.b13) if W.b13 is not None else np.zeros((E, 2 * N))
@@ -83,7 +83,7 @@ def dense_reference(wl, W, X, rsf=1.0):
     M = x.shape[0]
     Y = np.empty((E, M, K))
     for e in range(E):
-        h = rne_bf16(gs13[e] * (x @ W13[e].T) + b13[e])
+        h = gs13[e] * (x @ W13[e].T) + b13[e]
         g, u = h[:, :N], h[:, N:]
         if wl.act == "silu_mul":
             a = g / (1 + np.exp(-g)) * u
@@ -91,8 +91,7 @@ def dense_reference(wl, W, X, rsf=1.0):
             gc = np.minimum(g, wl.limit)
             uc = np.clip(u, -wl.limit, wl.limit)
             a = gc / (1 + np.exp(-wl.alpha * gc)) * (uc + 1)
-        a = rne_bf16(a)
-        Y[e] = rne_bf16(gs2[e] * (a @ W2[e].T) + b2[e])
+        Y[e] = gs2[e] * (a @ W2[e].T) + b2[e]
     out = np.zeros((M, K))
     if wl.post_norm:
         nw = rne_bf16(np.float32(1.0) + bf16v(X.post_norm_w).astype(np.float32))
@@ -132,10 +131,12 @@ def test_dense_bruteforce(orc, name):
     wl, W, X = make_small(name)
     got_bits, got_acc = orc.forward_workload(wl, W, X, return_acc=True)
     ref = dense_reference(wl, W, X)
-    # same rounding points, different loop structure: the pre-rounding sums
-    # agree to fp64 noise and the bf16 outputs agree bit for bit
-    np.testing.assert_allclose(got_acc, ref, rtol=1e-12, atol=1e-12)
-    np.testing.assert_array_equal(bf16v(got_bits), rne_bf16(ref))
+    # same arithmetic, different loop structure: the pre-rounding values agree to
+    # fp64 noise, and the bf16 outputs bit for bit except where that noise
+    # straddles a rounding boundary
+    np.testing.assert_allclose(got_acc, ref, rtol=1e-11, atol=1e-11)
+    same = bf16v(got_bits) == rne_bf16(ref)
+    assert same.mean() > 0.9999, same.mean()
     assert np.abs(ref).max() > 0.0
 
 
@@ -143,8 +144,8 @@ def test_dense_bruteforce(orc, name):
 @pytest.mark.parametrize("act", ["silu_mul", "sigmoid_alpha"])
 def test_closed_form_unit_scales(orc, fmt, act):
     """Unit scales, zero bias, every w13 code c1, every w2 code c2 and x in
-    {-1/8, 0, 1/8}: h = bf16(v1*S_t) on every row, a = bf16(act(h, h)),
-    y = bf16(v2*N*a), out_t = bf16(rsf * sum_j w_tj * y_t)."""
+    {-1/8, 0, 1/8}: h = v1*S_t on every row, a = act(h, h), y = v2*N*a,
+    out_t = bf16(rsf * sum_j w_tj * y_t)."""
     K, N, E, k, M = 128, 128, 3, 2, 6
     group = {"int4": 128, "mxfp4": 32, "nvfp4": 16}[fmt]
     wl = wk.Workload("closed", fmt, K=K, N=N, E=E, top_k=k, Ms=(M,), act=act)
@@ -166,18 +167,20 @@ def test_closed_form_unit_scales(orc, fmt, act):
     w = rng.uniform(0.1, 0.9, size=(M, k)).astype(np.float32)
     X = wk.BatchInputs(x, ids, w, None)
     rsf = 1.5
-    got = bf16v(orc.forward(W, X, act=act, rsf=rsf))
+    got_bits, got_acc = orc.forward(W, X, act=act, rsf=rsf, return_acc=True)
+    got = bf16v(got_bits)
     for t in range(M):
         S = xv[t].sum()
-        h = float(rne_bf16(np.array(v1 * S)))
+        h = v1 * S
         if act == "silu_mul":
             a = h / (1 + math.exp(-h)) * h
         else:
             a = h / (1 + math.exp(-1.702 * h)) * (h + 1)
-        a = float(rne_bf16(np.array(a)))
-        y = float(rne_bf16(np.array(v2 * N * a)))
-        expect = float(rne_bf16(np.array(rsf * float(w[t].astype(np.float64).sum()) * y)))
-        assert np.all(got[t] == expect), (t, got[t][:4], expect)
+        y = v2 * N * a
+        expect = rsf * float(w[t].astype(np.float64).sum()) * y
+        # fp64 evaluation order differs from the oracle's sums only in the last bits
+        np.testing.assert_allclose(got_acc[t], expect, rtol=1e-12, atol=1e-300)
+        assert np.all(got[t] == float(rne_bf16(np.array(expect)))), (t, got[t][:4], expect)
 
 
 @pytest.mark.parametrize("name", ["int4-bias-small", "nvfp4-ep-small", "mxfp4-alpha-small"])
