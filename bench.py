@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 fused-MoE layer on GB300.
+
+One step = one pass of the whole hot path (routing alignment, GEMM1 with the
+fused activation, GEMM2, combine) over one batch of seeded synthetic input,
+replayed from a CUDA graph with inputs resident in HBM; L2 is flushed (a
+write larger than L2) before every step and the step is bracketed by CUDA
+events.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME --M M]
+
+Under torchrun every rank runs an independent replica of the layer on its own
+GPU (the path has no cross-GPU exchange); value = all ranks' tokens / the
+slowest rank's time.  --impl reference times the CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from weight_only_bit_moe_gb300 import workloads as wk  # noqa: E402
+
+DEFAULT_WORKLOAD, DEFAULT_M = "int4-bias", 2304
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def touched_experts(wl, X) -> np.ndarray:
+    local = X.topk_ids.reshape(-1) - wl.expert_base
+    local = local[(local >= 0) & (local < wl.E)]
+    return np.unique(local)
+
+
+def local_pairs(wl, X) -> int:
+    local = X.topk_ids.reshape(-1) - wl.expert_base
+    return int(((local >= 0) & (local < wl.E)).sum())
+
+
+def algorithmic(wl, W, X):
+    """Bytes every step must move at least once and FLOPs over real pairs, per kernel."""
+    M = X.x.shape[0]
+    nt = len(touched_experts(wl, X))
+    P = local_pairs(wl, X)
+
+    def per_expert(a):
+        return 0 if a is None else a.nbytes // a.shape[0]
+
+    w13 = nt * (per_expert(W.w13) + per_expert(W.w13_s) + per_expert(W.b13) + (4 if W.w13_gs is not None else 0))
+    w2 = nt * (per_expert(W.w2) + per_expert(W.w2_s) + per_expert(W.b2) + (4 if W.w2_gs is not None else 0))
+    io = X.x.nbytes + M * wl.K * 2 + X.topk_ids.nbytes + X.topk_weights.nbytes
+    if wl.post_norm:
+        io += wl.K * 2
+    f1 = 2.0 * P * wl.K * 2 * wl.N
+    f2 = 2.0 * P * wl.N * wl.K
+    return {"bytes": w13 + w2 + io, "bytes_gemm1": w13 + X.x.nbytes, "bytes_gemm2": w2,
+            "flops": f1 + f2, "flops_gemm1": f1, "flops_gemm2": f2, "pairs": P, "touched": nt}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("common.cuh", "gemm.cuh", "gemm_launch.cuh"):
+        h.update(open(os.path.join(ROOT, "weight_only_bit_moe_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        e = d.get(f"{workload}:{kernel}")
+        if e and e.get("src_sha") == kernel_source_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        self.file.flush()
+        rows = []
+        try:
+            for line in open(self.file.name):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        finally:
+            os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank: int, world: int):
+    import torch
+
+    from weight_only_bit_moe_gb300 import binding, build
+    from weight_only_bit_moe_gb300.layer import MoELayer, batch_to_device
+
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(binding.LIB_PATH):
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    binding.load()
+
+    wl = wk.WORKLOADS[args.workload]
+    M = args.M
+    W = wk.make_weights(wl, wk.weight_seed(wl.name))
+    X = wk.make_batch(wl, M, wk.batch_seed(wl.name, M))
+    alg = algorithmic(wl, W, X)
+    layer = MoELayer.from_numpy(W, device=dev)
+    x, ids, tw, pnw = batch_to_device(X, dev)
+    pnw = pnw if wl.post_norm else None
+    B = args.block_m or layer.choose_block_m(M, wl.top_k, wl.n_ids)
+    a = layer.alloc_align(M, wl.top_k, B)
+    ws = layer.workspace(M, wl.top_k, B)
+    out = torch.empty((M, wl.K), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    kw = dict(expert_base=wl.expert_base, act=wl.act, alpha=wl.alpha, limit=wl.limit, post_norm_w=pnw,
+              norm_eps=wl.norm_eps, out=out, workspace=ws)
+
+    def step():
+        layer.align(ids, wl.expert_base, B, out=a)
+        layer.forward(x, ids, tw, a, **kw)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):  # eager warm-up: sets kernel attributes, caches device queries
+            step()
+        stream.synchronize()
+        if layer.status() != 0:
+            raise RuntimeError("device status not ok after warm-up")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        stream.synchronize()
+
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            graph.replay()
+        stream.synchronize()
+
+        # ---- timed region: K graph replays, L2 flushed before each, events around each
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local_rank) as clk:
+            for i in range(args.steps):
+                flush.fill_(1)
+                starts[i].record(stream)
+                graph.replay()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        clocks = clk.summary()
+
+        # ---- per-kernel times: traced eager steps, queued behind a spin so launches run ahead
+        tev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        kern = []
+        for i in range(args.steps):
+            flush.fill_(1)
+            torch.cuda._sleep(2_000_000)
+            binding.moe_set_trace_events(tev[i])
+            layer.align(ids, wl.expert_base, B, out=a)
+            layer.forward(x, ids, tw, a, **kw)
+            binding.moe_set_trace_events(None)
+        stream.synchronize()
+        for i in range(args.steps):
+            t = tev[i]
+            kern.append((t[0].elapsed_time(t[1]), t[1].elapsed_time(t[2]), t[2].elapsed_time(t[3])))
+        if layer.status() != 0:
+            raise RuntimeError("device status not ok after the timed steps")
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside
+    hx = torch.from_numpy(np.ascontiguousarray(X.x).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hids = torch.from_numpy(X.topk_ids.astype(np.int32)).pin_memory()
+    hw = torch.from_numpy(X.topk_weights.astype(np.float32)).pin_memory()
+    hout = torch.empty((M, wl.K), dtype=torch.bfloat16).pin_memory()
+    dx, dids, dw = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(tw)
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush.fill_(1)
+            stream.synchronize()
+            t0 = time.perf_counter()
+            dx.copy_(hx, non_blocking=True)
+            dids.copy_(hids, non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            aa = layer.align(dids, wl.expert_base, B, out=a)
+            layer.forward(dx, dids, dw, aa, **kw)
+            hout.copy_(out, non_blocking=True)
+            stream.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    h2d = hx.numel() * 2 + hids.numel() * 4 + hw.numel() * 4
+    d2h = hout.numel() * 2
+
+    # ---- reduce over ranks
+    ms = statistics.mean(step_ms)
+    e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([ms, e2e], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    g1 = statistics.mean(k[0] for k in kern)
+    g2 = statistics.mean(k[1] for k in kern)
+    cb = statistics.mean(k[2] for k in kern)
+    hbm, tc_burst, tc_sus, src = peaks()
+    t_hbm = alg["bytes"] / (hbm * 1e9)
+    t_tc = alg["flops"] / (tc_burst * 1e12)
+    tensor_bound = t_tc > t_hbm
+    dom = "gemm1" if g1 >= g2 else "gemm2"
+    dom_ms = g1 if dom == "gemm1" else g2
+    kname = f"moe_gemm_kernel<{wl.fmt},{'gated' if dom == 'gemm1' else 'plain'},BN={max(16, B)}>"
+    if tensor_bound:
+        achieved = alg[f"flops_{dom}"] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_burst, "unit": "TFLOP/s",
+                "frac": round(achieved / tc_burst, 4)}
+    else:
+        achieved = alg[f"bytes_{dom}"] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4)}
+    roof.update({"traffic": ncu_traffic(dom, f"{wl.name}:{M}"), "kernel": kname, "peak_source": src,
+                 "kernel_ms": round(dom_ms, 5)})
+
+    # ---- CPU oracle on a bounded sample of the same batch
+    cpu = cpu_baseline(wl, W, X, budget_s=args.cpu_budget)
+
+    value = world * M / (ms * 1e-3)
+    line = {
+        "metric": "MoE layer tokens/s", "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{wl.name} M={M}: {wl.fmt} W4A16, K={wl.K} N={wl.N} E={wl.E} top_k={wl.top_k} "
+                               f"group={wl.group}{' bias' if wl.bias_std else ''}, act={wl.act}"
+                               f"{', post-norm' if wl.post_norm else ''}, routed ids={wl.n_ids}, {wl.routing}",
+                   "M": M, "block_m": B, "parallelism": f"replicas x{world}", "l2": "flushed before every step",
+                   "graph": "CUDA graph replay"},
+        "roofline": roof,
+        "step_roofline": {"bytes": alg["bytes"], "flops": alg["flops"],
+                          "t_roof_us": round(max(t_hbm, t_tc) * 1e6, 3),
+                          "frac_of_step": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
+                          "bound": "tensor" if tensor_bound else "hbm"},
+        "kernels_ms": {"gemm1": round(g1, 5), "gemm2": round(g2, 5), "combine": round(cb, 5)},
+        "e2e": {"value": round(world * M / (e2e * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def cpu_baseline(wl, W, X, budget_s: float):
+    import oracle
+    oracle.build()
+    M = X.x.shape[0]
+    n = 1
+    t_used = 0.0
+    # grow the sample until it takes a few seconds, within the budget
+    while True:
+        toks = np.arange(min(n, M), dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.forward_workload(wl, W, X, tokens=toks)
+        dt = time.perf_counter() - t0
+        t_used += dt
+        if dt > 3.0 or n >= M or t_used + 4 * dt > budget_s:
+            break
+        n *= 4
+    return {"value": round(len(toks) / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"first {len(toks)} of {M} tokens, one pass, fp64 C oracle"}
+
+
+# ---------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = wk.WORKLOADS[args.workload]
+    M = args.M
+    W = wk.make_weights(wl, wk.weight_seed(wl.name))
+    X = wk.make_batch(wl, M, wk.batch_seed(wl.name, M))
+    per_step = min(M, args.ref_tokens)
+    times = []
+    for i in range(args.warmup + args.steps):
+        toks = (np.arange(per_step) + i * per_step) % M
+        t0 = time.perf_counter()
+        oracle.forward_workload(wl, W, X, tokens=toks.astype(np.int32))
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = per_step / (ms * 1e-3)
+    return {"metric": "MoE layer tokens/s", "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{wl.name} M={M}", "M": M, "sample_tokens_per_step": per_step},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": f"{per_step} of {M} tokens per step"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wk.WORKLOADS))
+    ap.add_argument("--M", type=int, default=DEFAULT_M)
+    ap.add_argument("--block-m", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        line = run_ours(args, rank, world)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * moe_w4a16.h -- C ABI of the GB300 (sm_103a) weight-only 4-bit fused
+ * Mixture-of-Experts layer.
+ *
+ * The layer is the expert computation of SGLang's Marlin MoE runner as the
+ * source pages describe it:
+ *   - "013-moe-middle-tiles.py" (open-kernel-challenge), kernel_fn: routing
+ *     alignment (moe_align_block_size) -> grouped GEMM1 against packed 4-bit
+ *     w13 -> silu_and_mul -> grouped GEMM2 against w2 -> post-expert-norm
+ *     weighted sum; Weights / Inputs / Config give the tensor layouts;
+ *   - "Marlin MoE kernel occupancy ..." (sglang PR #31552): the fused op
+ *     fused_marlin_moe(...) with per-expert bias (kHasBias) and the
+ *     expert-parallel block filter (kIsEP), and the per-expert reference loop of
+ *     test_fused_marlin_moe_large_non_ep_schedule (top-k weights applied in the
+ *     combine, tolerance |out - ref| <= 0.06 + 0.04 |ref|);
+ *   - "SM120 MXFP4 MoE ... Marlin" (sglang PR #28231): MXFP4 weights with GPT-OSS
+ *     interleaved gate/up rows (deinterleave_moe_mxfp4_w13_for_marlin), zero
+ *     padding of the intermediate dimension (_pad_w13/_pad_w2), the sigmoid-alpha
+ *     activation (swiglu_gpt_oss_sigmoid_alpha_contiguous) and the shape rule of
+ *     check_moe_marlin_supports_layer(allow_tile_padding): hidden % 64 == 0 and
+ *     intermediate % group_size == 0.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must point to memory the current CUDA
+ *     device can access; the caller owns all memory.  The library never
+ *     allocates device memory and never synchronises the stream, except where an
+ *     entry point says so.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All device work is enqueued on it, in order.
+ *   - Every entry point returns a moe_status.  Argument errors that the host can
+ *     see are returned synchronously and nothing is enqueued.  Errors found on the
+ *     device (a bounded wait that ran out) are recorded in the workspace status
+ *     word and reported by moe_get_status().
+ *   - Tensors are dense, row-major, with the shapes given below.
+ *   - bf16 values are passed as their 16-bit patterns.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = -1,      /* bad argument (null pointer, shape, enum, alignment) */
+    MOE_ERR_UNSUPPORTED = -2,  /* valid request this build does not implement */
+    MOE_ERR_CUDA = -3,         /* a CUDA runtime call failed */
+    MOE_ERR_TIMEOUT = -4,      /* a device-side bounded wait ran out */
+    MOE_ERR_WORKSPACE = -5     /* workspace too small */
+} moe_status;
+
+/* Weight formats.  Codes are 4 bits, two per byte, element 2j in the low nibble
+ * and element 2j+1 in the high nibble of byte j of a row.
+ *   INT4_U4B8: code q stands for q - 8 ("uint4b8"); one bf16 scale per group of
+ *              group_size (128) along the reduction dimension.
+ *   MXFP4:     E2M1 codes; one E8M0 scale byte (2^(b-127)) per 32.
+ *   NVFP4:     E2M1 codes; one FP8 E4M3 scale per 16, times one fp32 global
+ *              scale per expert (the same for gate and up rows). */
+typedef enum moe_wfmt { MOE_W_INT4_U4B8 = 0, MOE_W_MXFP4 = 1, MOE_W_NVFP4 = 2 } moe_wfmt;
+
+/* Gated activations; gate = first N outputs of GEMM1, up = the next N.
+ *   SILU_MUL:      silu(gate) * up                         (silu_and_mul)
+ *   SIGMOID_ALPHA: g = min(gate, limit), u = clamp(up, -limit, limit),
+ *                  g * sigmoid(alpha * g) * (u + 1)         (GPT-OSS) */
+typedef enum moe_act { MOE_ACT_SILU_MUL = 0, MOE_ACT_SIGMOID_ALPHA = 1 } moe_act;
+
+/* Shape of one layer's expert bank held by this GPU. */
+typedef struct moe_layer_desc {
+    int32_t fmt;              /* moe_wfmt */
+    int32_t num_experts;      /* E: experts held here, local ids 0..E-1 */
+    int32_t hidden;           /* K: model width (GEMM1 reduction, GEMM2 output); % 64 == 0, and
+                                 % 128 == 0 for INT4 */
+    int32_t inter;            /* N: expert intermediate width; % group_size == 0 */
+    int32_t group_size;       /* 128 (INT4), 32 (MXFP4) or 16 (NVFP4) */
+    int32_t w13_interleaved;  /* 1: w13 rows stored gate0, up0, gate1, up1, ... (GPT-OSS) */
+    int32_t has_bias13;       /* 1: per-expert bf16 bias on GEMM1 outputs */
+    int32_t has_bias2;        /* 1: per-expert bf16 bias on GEMM2 outputs */
+} moe_layer_desc;
+
+/* ------------------------------------------------------------------ repack
+ * Load-time conversion of checkpoint tensors into the kernels' tile-native
+ * layout ("013-moe-middle-tiles.py", prepare(): prepare_moe_nvfp4_layer_for_marlin;
+ * PR #28231: deinterleave, _pad_w13/_pad_w2).  One device pass; the output is an
+ * opaque blob of moe_repack_size() bytes that moe_w4a16_forward reads.
+ *
+ * Inputs (device pointers):
+ *   w13    uint8 [E, 2N, K/2]   packed codes (gate rows then up rows, or interleaved)
+ *   w13_s  [E, 2N, K/g]         bf16 (INT4) | uint8 E8M0 (MXFP4) | uint8 E4M3 (NVFP4)
+ *   w13_gs fp32 [E]             NVFP4 only, else NULL
+ *   b13    bf16 [E, 2N]         when has_bias13, else NULL (same row order as w13)
+ *   w2     uint8 [E, K, N/2];  w2_s [E, K, N/g];  w2_gs fp32 [E] (NVFP4);
+ *   b2     bf16 [E, K]          when has_bias2, else NULL
+ *   packed device buffer of moe_repack_size() bytes, 256-byte aligned.
+ * Returns MOE_ERR_INVALID for shapes outside the rules above or odd 2N rows
+ * when interleaved (the ValueError cases of deinterleave_moe_mxfp4_w13_for_marlin). */
+int64_t moe_repack_size(const moe_layer_desc* desc);
+int moe_repack_weights(const moe_layer_desc* desc, const void* w13, const void* w13_s,
+                       const float* w13_gs, const void* b13, const void* w2, const void* w2_s,
+                       const float* w2_gs, const void* b2, void* packed, void* stream);
+
+/* ------------------------------------------------------------------ align
+ * Routing alignment ("013-moe-middle-tiles.py", kernel_fn: moe_align_block_size;
+ * the -1 block marker of the PR #31552 kIsEP block filter).  Pair p = t*top_k + j
+ * with routed id topk_ids[p] is local when expert_base <= id < expert_base + E.
+ * Outputs (device):
+ *   sorted_ids int32 [cap]        local pairs grouped by expert (ascending local id),
+ *                                 ascending p within an expert, each expert's run
+ *                                 padded to a multiple of block_m with the sentinel
+ *                                 M*top_k; empty experts take no block; entries at
+ *                                 or past n_padded are the sentinel;
+ *   expert_ids int32 [cap/block_m] local expert of each block, -1 past n_padded;
+ *   n_padded   int32 [1]           sum over experts of ceil(count/block_m)*block_m.
+ * cap = moe_align_capacity(M, top_k, E, block_m) = roundup(M*top_k +
+ * min(E, M*top_k)*(block_m-1), block_m), the worst case over all routings.
+ * block_m must be 8, 16, 32, 64 or 128; E <= 1024; M*top_k < 2^31.
+ * topk_ids: int32 [M, top_k] device. */
+int64_t moe_align_capacity(int M, int top_k, int num_experts, int block_m);
+int moe_align(const int32_t* topk_ids, int M, int top_k, int expert_base, int num_experts,
+              int block_m, int32_t* sorted_ids, int32_t* expert_ids, int32_t* n_padded,
+              void* stream);
+
+/* Launch-configuration choice (host only, no device sync): the block_m the
+ * forward runs best with for this problem, from the token count, top_k, the
+ * number of experts routed ids range over and the layer shape.  Replaces the
+ * page's candidate loop ("013-moe-middle-tiles.py", BLOCK_SIZE_M_CANDIDATES). */
+int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, int num_routed_ids);
+
+/* ------------------------------------------------------------------ forward
+ * Workspace bytes moe_w4a16_forward needs for (desc, M, top_k, block_m); 256-byte
+ * aligned device memory owned by the caller; its contents need no initialisation. */
+int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int block_m);
+
+/* The layer ("013-moe-middle-tiles.py" kernel_fn after alignment; PR #31552
+ * fused_marlin_moe):
+ *   for every local pair p = (t, j) with expert e:
+ *     h = bf16(gs13[e] * x[t] . W13[e]^T + b13[e])            [2N]
+ *     a = bf16(act(h[:N], h[N:]))                              [N]
+ *     y = bf16(gs2[e] * a . W2[e]^T + b2[e])                   [K]
+ *   out[t] = bf16(rsf * sum_j topk_weights[t,j] * y_(t,j))      (post_norm_w == NULL)
+ *   out[t] = bf16(rsf * sum_j topk_weights[t,j] * inv_j * z_j),  z = y * nw,
+ *            nw = bf16(fp32(1 + post_norm_w)), inv = 1/sqrt(mean(z^2) + norm_eps)
+ *            (_expert_norm_factors / _expert_norm_sum, weight_first)
+ * Non-local pairs contribute nothing.
+ * Arguments (device unless said): packed from moe_repack_weights for `desc`;
+ * x bf16 [M, K]; topk_ids int32 [M, top_k]; topk_weights fp32 [M, top_k];
+ * sorted_ids / expert_ids / n_padded from moe_align with the same M, top_k,
+ * expert_base, E and block_m; act a moe_act; alpha, limit (host) for
+ * SIGMOID_ALPHA (limit = +inf: no clamp); post_norm_w bf16 [K] or NULL;
+ * out bf16 [M, K]; workspace of at least moe_workspace_size() bytes.
+ * M == 0 is a no-op. */
+int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void* x, int M,
+                      int top_k, const int32_t* topk_ids, const float* topk_weights,
+                      int expert_base, const int32_t* sorted_ids, const int32_t* expert_ids,
+                      const int32_t* n_padded, int block_m, int act, float alpha, float limit,
+                      float routed_scaling_factor, const void* post_norm_w, float norm_eps,
+                      void* out, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, returns the device status recorded in `workspace` by
+ * earlier forwards on it (MOE_OK or MOE_ERR_TIMEOUT) and clears it. */
+int moe_get_status(void* workspace, void* stream);
+
+/* Tracing hook.  With events != NULL and n == 4, every later moe_w4a16_forward
+ * records, on its stream, events[0] before GEMM1, events[1] between GEMM1 and
+ * GEMM2, events[2] between GEMM2 and the combine and events[3] after the
+ * combine, so a caller can time each kernel with cudaEventElapsedTime.
+ * events are cudaEvent_t handles created and owned by the caller; the table is
+ * copied.  NULL / 0 turns tracing off.  Process-wide, not thread-safe.
+ * Returns MOE_ERR_INVALID for any other n. */
+int moe_set_trace_events(void* const* events, int n);
+
+/* Short English name of a status code (static storage). */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_W4A16_H */

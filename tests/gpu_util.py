@@ -1,0 +1,78 @@
+"""Shared helpers for the GPU parity tests: build/load the library, run the
+layer through the C ABI, and compare with the oracle under the pages' bound."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from weight_only_bit_moe_gb300 import workloads as wk
+
+# |gpu - oracle| <= ATOL + RTOL * |oracle|, elementwise on bf16 outputs: the
+# assert_close(rtol=0.04, atol=0.06) of test_fused_marlin_moe_large_non_ep_schedule
+# in "Marlin MoE kernel occupancy ..." (sglang PR #31552).
+ATOL, RTOL = 0.06, 0.04
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from weight_only_bit_moe_gb300 import build, binding
+    build.build()
+    binding.load()
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def tensor_bf16_to_f32(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy()
+
+
+def check_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite GPU output"
+    assert np.all(np.isfinite(ref)), f"{what}: non-finite oracle output"
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    ratio = float((err / bound).max()) if err.size else 0.0
+    bad = np.argwhere(err > bound)
+    assert bad.size == 0, (f"{what}: {len(bad)} of {err.size} outside |d| <= {ATOL} + {RTOL}|ref|; "
+                           f"max err/bound {ratio:.3f}; first {bad[:5].tolist()} "
+                           f"got {got[tuple(bad[0])]:.5f} ref {ref[tuple(bad[0])]:.5f}")
+    return ratio
+
+
+def run_layer(layer, wl, X, block_m=None, **kw):
+    from weight_only_bit_moe_gb300.layer import batch_to_device
+    x, ids, w, pnw = batch_to_device(X)
+    out = layer(x, ids, w, expert_base=wl.expert_base, block_m=block_m, num_routed_ids=wl.n_ids,
+                act=wl.act, alpha=wl.alpha, limit=wl.limit, post_norm_w=pnw if wl.post_norm else None,
+                norm_eps=wl.norm_eps, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def sample_tokens(M: int, n: int, seed: int = 0) -> np.ndarray:
+    if M <= n:
+        return np.arange(M, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, M - 1), size=n - 2, replace=False)
+    return np.sort(np.concatenate([[0, M - 1], mid])).astype(np.int32)
+
+
+# Small variants of the workloads with shapes the kernels accept (hidden % 64,
+# int4 hidden % 128) that still span several tiles and a ragged tail: N below
+# the 128-row tile, hidden below the 256-row GEMM2 tile.
+GPU_SMALL = {
+    "tiny-int4": wk.WORKLOADS["tiny-int4"],
+    "int4-bias-small": dataclasses.replace(wk.WORKLOADS["int4-bias"], K=256, N=384, Ms=(37,)),
+    "mxfp4-alpha-small": dataclasses.replace(wk.WORKLOADS["mxfp4-alpha"], K=192, N=160, E=4, Ms=(29,)),
+    "mxfp4-alpha-clamp": dataclasses.replace(wk.WORKLOADS["mxfp4-alpha"], K=192, N=96, E=4, Ms=(13,), limit=7.0),
+    "nvfp4-ep-small": dataclasses.replace(wk.WORKLOADS["nvfp4-ep-norm"], K=320, N=48, E=4, E_global=16,
+                                          expert_base=4, Ms=(21,)),
+    "int4-zipf-small": dataclasses.replace(wk.WORKLOADS["int4-skew"], K=384, N=256, E=16, Ms=(50,)),
+}

@@ -1,0 +1,93 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds for
+sm_103a, loads, exports every function include/moe_w4a16.h declares, and
+rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from weight_only_bit_moe_gb300 import build, binding
+    build.build()
+    return binding
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe_w4a16.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    L = lib.load()
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(lib.EXPORTED)
+
+
+def test_capacity_matches_oracle(lib, orc):
+    for M, k, E, B in [(0, 2, 8, 16), (1, 8, 32, 16), (123, 2, 8, 16), (4096, 8, 128, 128), (7, 3, 1024, 8)]:
+        assert lib.moe_align_capacity(M, k, E, B) == orc.align_capacity(M, k, E, B)
+
+
+def test_repack_size_rules(lib):
+    D = lib.moe_layer_desc
+    assert lib.moe_repack_size(D(0, 8, 512, 1024, 128, 0, 1, 1)) > 0
+    assert lib.moe_repack_size(D(1, 32, 2880, 2880, 32, 1, 1, 1)) > 0     # tile padding allowed
+    assert lib.moe_repack_size(D(2, 32, 4096, 4096, 16, 0, 0, 0)) > 0
+    for bad in [D(0, 8, 512, 1024, 64, 0, 0, 0),      # wrong group for int4
+                D(0, 8, 576, 1024, 128, 0, 0, 0),     # int4 hidden % 128
+                D(1, 8, 2880, 2890, 32, 0, 0, 0),     # inter % group
+                D(1, 8, 2900, 2880, 32, 0, 0, 0),     # hidden % 64
+                D(3, 8, 512, 512, 16, 0, 0, 0),       # unknown format
+                D(2, 0, 512, 512, 16, 0, 0, 0)]:      # no experts
+        with pytest.raises(lib.MoeError):
+            lib.moe_repack_size(bad)
+
+
+def test_rejects_bad_arguments_without_device(lib):
+    L = lib.load()
+    # align: bad block_m, too many experts, null outputs -> MOE_ERR_INVALID before any CUDA call
+    assert L.moe_align(None, 4, 2, 0, 8, 24, 1, 1, 1, None) == lib.MOE_ERR_INVALID
+    assert L.moe_align(None, 4, 2, 0, 2000, 16, 1, 1, 1, None) == lib.MOE_ERR_INVALID
+    assert L.moe_align(1, 4, 2, 0, 8, 16, None, 1, 1, None) == lib.MOE_ERR_INVALID
+    d = lib.moe_layer_desc(0, 8, 512, 1024, 128, 0, 0, 0)
+    fwd = L.moe_w4a16_forward
+    args = [ctypes.byref(d), 256, 256, 4, 2, 8, 8, 0, 8, 8, 8, 16, 0, 1.0, 1.0, 1.0, None, 1e-8, 8, 256, 1 << 30,
+            None]
+    bad_act = list(args)
+    bad_act[12] = 7
+    assert fwd(*bad_act) == lib.MOE_ERR_INVALID
+    bad_bm = list(args)
+    bad_bm[11] = 24
+    assert fwd(*bad_bm) == lib.MOE_ERR_INVALID
+    bad_topk = list(args)
+    bad_topk[4] = 17
+    assert fwd(*bad_topk) == lib.MOE_ERR_INVALID
+    misaligned = list(args)
+    misaligned[1] = 257  # packed not 256-byte aligned
+    assert fwd(*misaligned) == lib.MOE_ERR_INVALID
+    zero = list(args)
+    zero[3] = 0          # M == 0 is a no-op
+    assert fwd(*zero) == lib.MOE_OK
+    assert lib.status_string(lib.MOE_ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_block_m_chooser(lib):
+    d = lib.moe_layer_desc(0, 128, 4096, 1536, 128, 0, 0, 0)
+    assert lib.moe_choose_block_m(d, 1, 8, 128) == 16
+    assert lib.moe_choose_block_m(d, 16, 8, 128) == 16
+    assert lib.moe_choose_block_m(d, 4096, 8, 128) == 128
+    # monotone in the token count
+    prev = 0
+    for M in [1, 2, 8, 32, 128, 512, 1024, 4096, 65536]:
+        b = lib.moe_choose_block_m(d, M, 8, 128)
+        assert b >= prev and b in (8, 16, 32, 64, 128)
+        prev = b

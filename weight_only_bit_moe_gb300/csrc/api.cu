@@ -1,0 +1,241 @@
+// Host side of the C ABI: argument checks, the launch-configuration chooser,
+// the workspace plan and the forward's launch sequence (GEMM1 + activation ->
+// GEMM2 -> combine), all enqueued on the caller's stream without host syncs.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "combine.cuh"
+#include "gemm_launch.cuh"
+
+namespace moe {
+
+constexpr int64_t kSplitBudgetBytes = 64ll << 20;  // cap on each split-K partial area
+constexpr int kMaxSplit = 16;
+
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Everything the forward places in the caller's workspace, in bytes from its start.
+struct WsPlan {
+  int64_t cap, blocks;
+  int grid;
+  int max_split1, max_split2, rows1, rows2;
+  int64_t status_off, counters_off, counters_bytes, a_off, y_off, inv_off, part1_off, part2_off, total;
+};
+
+bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w) {
+  const int64_t cap = moe_align_capacity(M, top_k, L.E, block_m);
+  if (cap < 0) return false;
+  const int grid = device_sm_count();
+  if (grid <= 0) return false;
+  const int64_t pairs = (int64_t)M * top_k;
+  w->cap = cap;
+  w->blocks = cap / block_m;
+  w->grid = grid;
+  // split-K only runs while tiles * blocks < grid, so the partial rows stay below this bound
+  w->rows1 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T1 + 1) * block_m);
+  w->rows2 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T2 + 1) * block_m);
+  const int64_t per1 = (int64_t)w->rows1 * 2 * L.Npad * 4, per2 = (int64_t)w->rows2 * L.K * 4;
+  w->max_split1 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per1 ? kSplitBudgetBytes / per1 : 1));
+  w->max_split2 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per2 ? kSplitBudgetBytes / per2 : 1));
+  int64_t off = 0;
+  w->status_off = off;
+  off += 256;
+  w->counters_off = off;
+  w->counters_bytes = (int64_t)L.T1 * w->blocks * 4;
+  off = round_up64(off + w->counters_bytes, 256);
+  w->a_off = off;
+  off = round_up64(off + cap * L.Npad * 2, 256);
+  w->y_off = off;
+  off = round_up64(off + pairs * L.K * 4, 256);
+  w->inv_off = off;
+  off = round_up64(off + pairs * 4, 256);
+  w->part1_off = off;
+  off = round_up64(off + (int64_t)w->max_split1 * per1, 256);
+  w->part2_off = off;
+  off = round_up64(off + (int64_t)w->max_split2 * per2, 256);
+  w->total = off;
+  return true;
+}
+
+cudaError_t launch_gemm(int fmt, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
+  switch (fmt) {
+    case MOE_W_INT4_U4B8: return launch_gemm_int4(gated, bn, g, grid, st);
+    case MOE_W_MXFP4: return launch_gemm_mxfp4(gated, bn, g, grid, st);
+    case MOE_W_NVFP4: return launch_gemm_nvfp4(gated, bn, g, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+bool valid_block_m(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128; }
+
+cudaEvent_t g_trace[4] = {nullptr, nullptr, nullptr, nullptr};
+bool g_tracing = false;
+
+inline cudaError_t trace(int i, cudaStream_t st) {
+  return g_tracing ? cudaEventRecord(g_trace[i], st) : cudaSuccess;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, int num_routed_ids) {
+  if (!desc || M < 0 || top_k <= 0 || num_routed_ids <= 0) return MOE_ERR_INVALID;
+  // expected rows per local expert: routed pairs spread over the routed id range
+  const double rows = (double)M * top_k / (double)num_routed_ids;
+  if (rows <= 16.0) return 16;
+  if (rows <= 32.0) return 32;
+  if (rows <= 96.0) return 64;
+  return 128;
+}
+
+extern "C" int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int block_m) {
+  Layout L;
+  WsPlan w;
+  if (!desc || !make_layout(*desc, &L) || M < 0 || top_k <= 0 || !valid_block_m(block_m)) return -1;
+  if (!plan_workspace(L, M, top_k, block_m, &w)) return -1;
+  return w.total;
+}
+
+extern "C" int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void* x, int M, int top_k,
+                                 const int32_t* topk_ids, const float* topk_weights, int expert_base,
+                                 const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* n_padded,
+                                 int block_m, int act, float alpha, float limit, float routed_scaling_factor,
+                                 const void* post_norm_w, float norm_eps, void* out, void* workspace,
+                                 int64_t workspace_bytes, void* stream) {
+  Layout L;
+  if (!desc || !make_layout(*desc, &L)) return MOE_ERR_INVALID;
+  if (M < 0 || top_k <= 0 || top_k > 16 || !valid_block_m(block_m)) return MOE_ERR_INVALID;
+  if (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SIGMOID_ALPHA) return MOE_ERR_INVALID;
+  if ((int64_t)M * top_k >= (int64_t)1 << 31) return MOE_ERR_INVALID;
+  if (M == 0) return MOE_OK;
+  if (!packed || !x || !topk_ids || !topk_weights || !sorted_ids || !expert_ids || !n_padded || !out ||
+      !workspace)
+    return MOE_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(packed) & 255) || (reinterpret_cast<uintptr_t>(workspace) & 255) ||
+      (reinterpret_cast<uintptr_t>(x) & 15))
+    return MOE_ERR_INVALID;
+  WsPlan w;
+  if (!plan_workspace(L, M, top_k, block_m, &w)) return MOE_ERR_CUDA;
+  if (workspace_bytes < w.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  const int bn = block_m < 16 ? 16 : block_m;
+
+  // status word, chosen split and split-K arrival counters start at zero every call
+  if (cudaMemsetAsync(ws, 0, w.counters_off + w.counters_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (trace(0, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmArgs g{};
+  g.L = L;
+  g.packed = pk;
+  g.sorted_ids = sorted_ids;
+  g.expert_ids = expert_ids;
+  g.n_padded = n_padded;
+  g.pairs = M * top_k;
+  g.top_k = top_k;
+  g.block_m = block_m;
+  g.act_kind = act;
+  g.alpha = alpha;
+  g.limit = limit;
+  g.a_out = reinterpret_cast<uint16_t*>(ws + w.a_off);
+  g.y_out = reinterpret_cast<float*>(ws + w.y_off);
+  g.inv_pos = reinterpret_cast<int32_t*>(ws + w.inv_off);
+  g.counters = reinterpret_cast<int32_t*>(ws + w.counters_off);
+  g.split_used = reinterpret_cast<int32_t*>(ws + w.status_off + 4);
+  g.status = reinterpret_cast<unsigned*>(ws + w.status_off);
+
+  // GEMM1 + activation
+  g.act = static_cast<const uint16_t*>(x);
+  g.act_ld = L.K;
+  g.has_bias = desc->has_bias13 != 0;
+  g.max_split = w.max_split1;
+  g.split_rows = w.rows1;
+  g.partial = reinterpret_cast<float*>(ws + w.part1_off);
+  if (launch_gemm(L.fmt, true, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (trace(1, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // GEMM2
+  g.act = g.a_out;
+  g.act_ld = L.Npad;
+  g.has_bias = desc->has_bias2 != 0;
+  g.max_split = w.max_split2;
+  g.split_rows = w.rows2;
+  g.partial = reinterpret_cast<float*>(ws + w.part2_off);
+  if (launch_gemm(L.fmt, false, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (trace(2, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // combine
+  CombineArgs c{};
+  c.M = M;
+  c.top_k = top_k;
+  c.K = L.K;
+  c.Kpad2 = L.Kpad2;
+  c.expert_base = expert_base;
+  c.E = L.E;
+  c.topk_ids = topk_ids;
+  c.topk_weights = topk_weights;
+  c.y = reinterpret_cast<const float*>(ws + w.y_off);
+  c.partial = reinterpret_cast<const float*>(ws + w.part2_off);
+  c.split_rows = w.rows2;
+  c.split_used = g.split_used;
+  c.inv_pos = g.inv_pos;
+  c.gs2 = reinterpret_cast<const float*>(pk + L.gs2_off);
+  c.b2 = desc->has_bias2 ? reinterpret_cast<const uint16_t*>(pk + L.b2_off) : nullptr;
+  c.post_norm_w = static_cast<const uint16_t*>(post_norm_w);
+  c.norm_eps = norm_eps;
+  c.rsf = routed_scaling_factor;
+  c.out = static_cast<uint16_t*>(out);
+  if (launch_combine(c, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (trace(3, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+extern "C" int moe_set_trace_events(void* const* events, int n) {
+  if (!events || n == 0) {
+    g_tracing = false;
+    return MOE_OK;
+  }
+  if (n != 4) return MOE_ERR_INVALID;
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return MOE_ERR_INVALID;
+    g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_tracing = true;
+  return MOE_OK;
+}
+
+extern "C" int moe_get_status(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned v = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+extern "C" const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}

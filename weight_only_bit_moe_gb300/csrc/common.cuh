@@ -1,0 +1,375 @@
+// Device helpers and the tile-native packed-weight layout shared by the repack
+// and GEMM kernels of the W4A16 fused-MoE library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_w4a16.h"
+
+namespace moe {
+
+// ----------------------------------------------------------------------------
+// Packed weight layout.
+//
+// Both grouped GEMMs compute 256 weight rows per CTA tile as two 128-row MMA
+// operands ("halves").  GEMM1 tile i holds gate rows [128i, 128i+128) in half 0
+// and the matching up rows in half 1, so one TMEM lane holds the gate and up
+// value of the same intermediate feature and the activation runs in the GEMM1
+// epilogue.  GEMM2 tile i holds output rows [256i, 256i+256).  N is zero-padded
+// to Npad = roundup(N, 128) and GEMM2's rows to roundup(K, 256) (the pages'
+// _pad_w13/_pad_w2 tile padding); padded codes decode to 0.
+//
+// Each tile is a sequence of K-stages of 64 reduction elements.  A stage's
+// packed codes are 8 KiB: uint4 units [j][r] (j = 0,1 is the 32-element half of
+// the stage, r the tile row), so that thread r of the dequant warps reads
+// units r and 256 + r, both conflict-free.  Inside one 32-bit word (8 elements
+// e0..e7 of a row), element 2i sits at bits 4i and element 2i+1 at bits 16+4i:
+// one shift and mask yields a bf16x2 pair of consecutive elements.
+//
+// Scales ride in front of the stage that first needs them: INT4 (one bf16 per
+// 128 = two stages) only in front of even stages, 256 x bf16; MXFP4 two E8M0
+// bytes per row per stage (256 x u16); NVFP4 four E4M3 bytes (256 x u32).
+// ----------------------------------------------------------------------------
+constexpr int kTileRows = 256;       // weight rows per CTA tile (2 x 128)
+constexpr int kStageK = 64;          // reduction elements per stage
+constexpr int kPackedStageBytes = kTileRows * kStageK / 2;  // 8192
+
+struct Layout {
+  int fmt, E, K, N, group;
+  int Npad;        // roundup(N, 128)
+  int Kpad2;       // roundup(K, 256)
+  int T1, T2;      // GEMM1 tiles (Npad/128), GEMM2 tiles (Kpad2/256)
+  int S1, S2;      // stages per tile: K/64 and Npad/64
+  int period;      // stages per scale chunk: 2 (INT4) or 1
+  int scale_bytes; // scale bytes per chunk
+  int64_t period_bytes;   // scale_bytes + period * 8192
+  int64_t tile1_bytes, tile2_bytes;
+  int64_t w13_off, w2_off, b13_off, b2_off, gs13_off, gs2_off, total;
+};
+
+__host__ __device__ inline int64_t round_up64(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+__host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
+  if (d.fmt < 0 || d.fmt > 2 || d.num_experts <= 0 || d.hidden <= 0 || d.inter <= 0) return false;
+  const int want_group = d.fmt == MOE_W_INT4_U4B8 ? 128 : (d.fmt == MOE_W_MXFP4 ? 32 : 16);
+  if (d.group_size != want_group) return false;
+  if (d.hidden % 64 || d.inter % d.group_size) return false;
+  if (d.fmt == MOE_W_INT4_U4B8 && d.hidden % 128) return false;
+  L->fmt = d.fmt;
+  L->E = d.num_experts;
+  L->K = d.hidden;
+  L->N = d.inter;
+  L->group = d.group_size;
+  L->Npad = (int)round_up64(d.inter, 128);
+  L->Kpad2 = (int)round_up64(d.hidden, 256);
+  L->T1 = L->Npad / 128;
+  L->T2 = L->Kpad2 / 256;
+  L->S1 = d.hidden / kStageK;
+  L->S2 = L->Npad / kStageK;
+  L->period = d.fmt == MOE_W_INT4_U4B8 ? 2 : 1;
+  L->scale_bytes = kTileRows * (d.fmt == MOE_W_NVFP4 ? 4 : 2);
+  L->period_bytes = L->scale_bytes + (int64_t)L->period * kPackedStageBytes;
+  L->tile1_bytes = (int64_t)(L->S1 / L->period) * L->period_bytes;
+  L->tile2_bytes = (int64_t)(L->S2 / L->period) * L->period_bytes;
+  int64_t off = 256;  // 256-byte header (reserved)
+  L->w13_off = off;
+  off += (int64_t)L->E * L->T1 * L->tile1_bytes;
+  L->w2_off = off = round_up64(off, 256);
+  off += (int64_t)L->E * L->T2 * L->tile2_bytes;
+  L->b13_off = off = round_up64(off, 256);
+  if (d.has_bias13) off += (int64_t)L->E * 2 * L->Npad * 2;
+  L->b2_off = off = round_up64(off, 256);
+  if (d.has_bias2) off += (int64_t)L->E * L->Kpad2 * 2;
+  L->gs13_off = off = round_up64(off, 256);
+  off += (int64_t)L->E * 4;
+  L->gs2_off = off = round_up64(off, 256);
+  off += (int64_t)L->E * 4;
+  L->total = round_up64(off, 256);
+  return true;
+}
+
+// Byte offset of stage s inside a tile, whether it carries scales, and its size.
+__host__ __device__ inline int64_t stage_offset(const Layout& L, int s) {
+  const int q = s / L.period, r = s % L.period;
+  return q * L.period_bytes + (r == 0 ? 0 : L.scale_bytes + (int64_t)r * kPackedStageBytes);
+}
+__host__ __device__ inline bool stage_has_scales(const Layout& L, int s) { return s % L.period == 0; }
+__host__ __device__ inline int stage_bytes(const Layout& L, int s) {
+  return kPackedStageBytes + (stage_has_scales(L, s) ? L.scale_bytes : 0);
+}
+
+// Epilogue factor applied to fp32 accumulators.  FP4 formats dequantise to
+// value * 2^-8 (see dequant below), NVFP4 also carries its global scale.
+constexpr float kFp4Unscale = 256.0f;
+
+// ----------------------------------------------------------------------------
+// Device status word (first 4 bytes of the forward workspace).
+// ----------------------------------------------------------------------------
+constexpr unsigned kStatusTimeout = 1u;
+
+// ----------------------------------------------------------------------------
+// PTX wrappers.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Gives up after
+// kWaitLimitNs, records kStatusTimeout in *status, raises the CTA's abort flag
+// and returns false; once the flag is up, later waits return at once, so a CTA
+// that lost a producer still leaves in bounded time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completing on an mbarrier (transaction bytes).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (tensor core) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on bar when all previously issued tcgen05 ops of this thread are done.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+// 32 TMEM lanes x 16 consecutive 32-bit columns; lane = warp quarter + thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzled
+// canonical layout: rows of 128 bytes (64 bf16 of one K-stage), 8-row atoms of
+// 1024 bytes (stride-dimension offset), 16-byte chunk c of row r stored at chunk
+// c ^ (r % 8).  The atom base must be 1024-byte aligned; advancing the start
+// address by 32 bytes selects the next K=16 slice.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+  d |= (uint64_t)1 << 16;                          // leading-dim offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                // stride-dim offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                          // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                          // swizzle: 128 B
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A and B both fp16 (ab_bf16 = 0) or both
+// bf16 (ab_bf16 = 1), D = fp32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, uint32_t ab_bf16) {
+  return (1u << 4)                         // D format fp32
+         | (ab_bf16 << 7)                  // A format
+         | (ab_bf16 << 10)                 // B format
+         | ((uint32_t)(N >> 3) << 17)      // N / 8
+         | ((uint32_t)(M >> 4) << 24);     // M / 16
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r in a SW128 K-major tile.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+  return (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- bf16 bits
+__device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __nv_bfloat162 bits_bf162(uint32_t u) { return *reinterpret_cast<__nv_bfloat162*>(&u); }
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+__device__ __forceinline__ float round_bf16(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
+
+// ---------------------------------------------------------------- dequant
+// Per-stage scale multipliers of one row, as bf16x2 (same value in both lanes).
+// INT4: the bf16 scale itself.  FP4: the block scale times 2^118 (E2M1 codes are
+// decoded as bf16 patterns that stand for value * 2^-126, see below; the product
+// is then value * scale * 2^-8, undone in the epilogue by kFp4Unscale).
+__device__ __forceinline__ uint32_t e8m0_mult_bits(uint32_t b) {
+  // 2^(b-127) * 2^118 = 2^(b-9): bf16 exponent field b - 9 + 127 = b + 118
+  return ((b + 118u) & 0xFFu) << 7;
+}
+__device__ __forceinline__ uint32_t e4m3_mult_bits(uint32_t b) {
+  // value(b) * 2^118 computed in fp32 (exact), then as bf16 (exact: 4 significant bits)
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;  // m/8 * 2^-6
+  v *= 3.3230699894622794e35f;  // 2^118
+  return (__float_as_uint(v) >> 16) & 0x7FFFu;
+}
+
+// ---- fp16 operands (every format): exact for all three, since (q - 8) * s has
+// at most 11 significant bits and E2M1 x scale at most 6.
+// INT4 (uint4b8): pair i of word w -> f16x2 (q - 8) * s, s the scale as fp16.
+__device__ __forceinline__ uint32_t dq_int4_pair_f16(uint32_t w, int i, uint32_t s2) {
+  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;  // 1024 + q, exact
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+  const __half2 r = __hmul2(v, *reinterpret_cast<const __half2*>(&s2));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+// E2M1: sign -> bit 15, exponent/mantissa -> bits 11..9 of the fp16 pattern,
+// i.e. the pattern of value * 2^-14 (0.5 is an fp16 subnormal, exact), times
+// the multiplier scale * 2^6, giving value * scale * 2^-8.
+__device__ __forceinline__ uint32_t dq_e2m1_pair_f16(uint32_t w, int i, uint32_t m2) {
+  const uint32_t t = w >> (4 * i);
+  const uint32_t p = ((t << 9) & 0x0E000E00u) | ((t << 12) & 0x80008000u);
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&p), *reinterpret_cast<const __half2*>(&m2));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t e8m0_mult_f16(uint32_t b) {
+  // 2^(b-127) * 2^6 = 2^(b-121): fp16 exponent field b - 106 (b in [107, 136])
+  return ((b - 106u) & 0x1Fu) << 10;
+}
+__device__ __forceinline__ uint32_t e4m3_mult_f16(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+  return __half_as_ushort(__float2half_rn(v * 64.0f));
+}
+__device__ __forceinline__ uint32_t bf16_scale_f16(uint32_t sbits) {
+  return __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
+}
+// 8 bf16 -> 8 fp16 (round to nearest; exact inside the fp16 range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// ---- bf16 operands (FP4 formats in GEMM1, whose B operand is the bf16 input).
+// INT4 (uint4b8): pair i of word w -> bf16x2 (q - 8) * s.
+__device__ __forceinline__ uint32_t dq_int4_pair(uint32_t w, int i, uint32_t s2) {
+  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;  // 128 + q, exact
+  const __nv_bfloat162 v = __hsub2(bits_bf162(t), bits_bf162(0x43084308u));  // - 136 -> q - 8, exact
+  return bf162_bits(__hmul2(v, bits_bf162(s2)));
+}
+// E2M1: sign -> bit 15, exponent/mantissa -> bits 8..6 of the bf16 pattern,
+// i.e. the pattern of value * 2^-126 (E2M1's subnormal 0.5 maps to a bf16
+// subnormal, exact), then times the multiplier.
+__device__ __forceinline__ uint32_t dq_e2m1_pair(uint32_t w, int i, uint32_t m2) {
+  const uint32_t t = w >> (4 * i);
+  const uint32_t p = ((t << 6) & 0x01C001C0u) | ((t << 12) & 0x80008000u);
+  return bf162_bits(__hmul2(bits_bf162(p), bits_bf162(m2)));
+}
+
+}  // namespace moe

@@ -1,0 +1,213 @@
+// Load-time repack of checkpoint expert weights into the tile-native layout
+// described in common.cuh ("013-moe-middle-tiles.py", prepare():
+// prepare_moe_nvfp4_layer_for_marlin; "SM120 MXFP4 MoE ... Marlin" (sglang
+// PR #28231): deinterleave_moe_mxfp4_w13_for_marlin, _pad_w13 / _pad_w2).
+//
+// Every output byte is written by exactly one thread; reading the source is
+// byte-gather work, so the kernels are simple and run once per layer.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct RepackArgs {
+  Layout L;
+  int interleaved, has_b13, has_b2;
+  const uint8_t* w13;
+  const uint8_t* w13_s;
+  const float* w13_gs;
+  const uint16_t* b13;
+  const uint8_t* w2;
+  const uint8_t* w2_s;
+  const float* w2_gs;
+  const uint16_t* b2;
+  uint8_t* out;
+};
+
+// Source row of tile row r for matrix `which` (0 = w13, 1 = w2), or -1 for a
+// padding row.  w13: half 0 = gate, half 1 = up; interleaved storage keeps gate
+// i in row 2i and up i in row 2i+1.
+__device__ __forceinline__ int source_row(const RepackArgs& a, int which, int tile, int r) {
+  const Layout& L = a.L;
+  if (which == 0) {
+    const int f = tile * 128 + (r & 127), half = r >> 7;
+    if (f >= L.N) return -1;
+    return a.interleaved ? 2 * f + half : half * L.N + f;
+  }
+  const int c = tile * kTileRows + r;
+  return c < L.K ? c : -1;
+}
+
+__device__ __forceinline__ uint32_t zero_code(int fmt) { return fmt == MOE_W_INT4_U4B8 ? 8u : 0u; }
+
+// One thread per 16-byte unit of packed codes: unit (e, tile, stage, j, r).
+__global__ void repack_codes_kernel(RepackArgs a, int which) {
+  const Layout& L = a.L;
+  const int T = which ? L.T2 : L.T1, S = which ? L.S2 : L.S1;
+  const int red = which ? L.N : L.K;  // real reduction length
+  const int64_t units = (int64_t)L.E * T * S * 512;
+  const int64_t tile_bytes = which ? L.tile2_bytes : L.tile1_bytes;
+  const uint8_t* src = which ? a.w2 : a.w13;
+  const int64_t src_row_bytes = red / 2;
+  const int64_t src_rows = which ? L.K : 2 * L.N;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(u % 256);
+    const int j = (int)((u / 256) % 2);
+    const int s = (int)((u / 512) % S);
+    const int tile = (int)((u / (512LL * S)) % T);
+    const int e = (int)(u / (512LL * S * T));
+    const int row = source_row(a, which, tile, r);
+    const uint8_t* srow = row >= 0 ? src + ((int64_t)e * src_rows + row) * src_row_bytes : nullptr;
+    uint32_t words[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int el = 0; el < 8; ++el) {
+        const int k = s * kStageK + 32 * j + 8 * w + el;
+        uint32_t q = zero_code(L.fmt);
+        if (srow && k < red) {
+          const uint8_t b = srow[k >> 1];
+          q = (k & 1) ? (b >> 4) : (b & 15u);
+        }
+        const int pos = (el & 1) ? 16 + 4 * (el >> 1) : 4 * (el >> 1);
+        word |= q << pos;
+      }
+      words[w] = word;
+    }
+    uint8_t* dst = a.out + (which ? L.w2_off : L.w13_off) + ((int64_t)e * T + tile) * tile_bytes +
+                   stage_offset(L, s) + (stage_has_scales(L, s) ? L.scale_bytes : 0) + ((int64_t)j * 256 + r) * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+  }
+}
+
+// One thread per (e, tile, scale chunk, row): 2 or 4 bytes of scales.
+__global__ void repack_scales_kernel(RepackArgs a, int which) {
+  const Layout& L = a.L;
+  const int T = which ? L.T2 : L.T1, S = which ? L.S2 : L.S1;
+  const int chunks = S / L.period;
+  const int red = which ? L.N : L.K;
+  const int groups = red / L.group;  // real groups per source row
+  const int64_t total = (int64_t)L.E * T * chunks * 256;
+  const int64_t tile_bytes = which ? L.tile2_bytes : L.tile1_bytes;
+  const uint8_t* src = which ? a.w2_s : a.w13_s;
+  const int64_t src_rows = which ? L.K : 2 * L.N;
+  const int sb = L.fmt == MOE_W_INT4_U4B8 ? 2 : 1;  // source bytes per scale
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(u % 256);
+    const int q = (int)((u / 256) % chunks);
+    const int tile = (int)((u / (256LL * chunks)) % T);
+    const int e = (int)(u / (256LL * chunks * T));
+    const int row = source_row(a, which, tile, r);
+    const uint8_t* srow = row >= 0 ? src + ((int64_t)e * src_rows + row) * groups * sb : nullptr;
+    uint8_t* dst = a.out + (which ? L.w2_off : L.w13_off) + ((int64_t)e * T + tile) * tile_bytes +
+                   stage_offset(L, q * L.period);
+    if (L.fmt == MOE_W_INT4_U4B8) {  // group q covers stages 2q, 2q+1
+      uint16_t v = 0x3F80;            // 1.0 for padding
+      if (srow && q < groups) v = reinterpret_cast<const uint16_t*>(srow)[q];
+      reinterpret_cast<uint16_t*>(dst)[r] = v;
+    } else if (L.fmt == MOE_W_MXFP4) {  // groups 2q, 2q+1 (32 each)
+      uint32_t v = 0;
+      for (int g = 0; g < 2; ++g) {
+        const int gi = 2 * q + g;
+        uint32_t b = 127;  // 2^0 for padding
+        if (srow && gi < groups) b = srow[gi];
+        v |= b << (8 * g);
+      }
+      reinterpret_cast<uint16_t*>(dst)[r] = (uint16_t)v;
+    } else {  // NVFP4: groups 4q .. 4q+3 (16 each)
+      uint32_t v = 0;
+      for (int g = 0; g < 4; ++g) {
+        const int gi = 4 * q + g;
+        uint32_t b = 0x38;  // 1.0 for padding
+        if (srow && gi < groups) b = srow[gi];
+        v |= b << (8 * g);
+      }
+      reinterpret_cast<uint32_t*>(dst)[r] = v;
+    }
+  }
+}
+
+// Bias rows (deinterleaved, zero padded) and global scales.
+__global__ void repack_misc_kernel(RepackArgs a) {
+  const Layout& L = a.L;
+  const int64_t n13 = a.has_b13 ? (int64_t)L.E * 2 * L.Npad : 0;
+  const int64_t n2 = a.has_b2 ? (int64_t)L.E * L.Kpad2 : 0;
+  const int64_t ngs = L.E;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < n13 + n2 + ngs;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    if (u < n13) {
+      const int f = (int)(u % L.Npad), half = (int)((u / L.Npad) % 2), e = (int)(u / (2LL * L.Npad));
+      uint16_t v = 0;
+      if (f < L.N) {
+        const int row = a.interleaved ? 2 * f + half : half * L.N + f;
+        v = a.b13[(int64_t)e * 2 * L.N + row];
+      }
+      reinterpret_cast<uint16_t*>(a.out + L.b13_off)[u] = v;
+    } else if (u < n13 + n2) {
+      const int64_t v2 = u - n13;
+      const int c = (int)(v2 % L.Kpad2), e = (int)(v2 / L.Kpad2);
+      reinterpret_cast<uint16_t*>(a.out + L.b2_off)[v2] = c < L.K ? a.b2[(int64_t)e * L.K + c] : (uint16_t)0;
+    } else {
+      const int e = (int)(u - n13 - n2);
+      float g13 = 1.0f, g2 = 1.0f;
+      if (L.fmt == MOE_W_NVFP4) {
+        g13 = a.w13_gs[e];
+        g2 = a.w2_gs[e];
+      }
+      if (L.fmt != MOE_W_INT4_U4B8) {
+        g13 *= kFp4Unscale;
+        g2 *= kFp4Unscale;
+      }
+      reinterpret_cast<float*>(a.out + L.gs13_off)[e] = g13;
+      reinterpret_cast<float*>(a.out + L.gs2_off)[e] = g2;
+    }
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int64_t moe_repack_size(const moe_layer_desc* desc) {
+  Layout L;
+  if (!desc || !make_layout(*desc, &L)) return -1;
+  return L.total;
+}
+
+extern "C" int moe_repack_weights(const moe_layer_desc* desc, const void* w13, const void* w13_s,
+                                  const float* w13_gs, const void* b13, const void* w2, const void* w2_s,
+                                  const float* w2_gs, const void* b2, void* packed, void* stream) {
+  Layout L;
+  if (!desc || !make_layout(*desc, &L)) return MOE_ERR_INVALID;
+  if (!w13 || !w13_s || !w2 || !w2_s || !packed) return MOE_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(packed) & 255) != 0) return MOE_ERR_INVALID;
+  if (desc->fmt == MOE_W_NVFP4 && (!w13_gs || !w2_gs)) return MOE_ERR_INVALID;
+  if ((desc->has_bias13 && !b13) || (desc->has_bias2 && !b2)) return MOE_ERR_INVALID;
+  if (desc->w13_interleaved && (2 * desc->inter) % 2 != 0) return MOE_ERR_INVALID;
+  RepackArgs a;
+  a.L = L;
+  a.interleaved = desc->w13_interleaved != 0;
+  a.has_b13 = desc->has_bias13 != 0;
+  a.has_b2 = desc->has_bias2 != 0;
+  a.w13 = static_cast<const uint8_t*>(w13);
+  a.w13_s = static_cast<const uint8_t*>(w13_s);
+  a.w13_gs = w13_gs;
+  a.b13 = static_cast<const uint16_t*>(b13);
+  a.w2 = static_cast<const uint8_t*>(w2);
+  a.w2_s = static_cast<const uint8_t*>(w2_s);
+  a.w2_gs = w2_gs;
+  a.b2 = static_cast<const uint16_t*>(b2);
+  a.out = static_cast<uint8_t*>(packed);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(packed, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;  // header
+  const int threads = 256, blocks = 152 * 16;
+  for (int which = 0; which < 2; ++which) {
+    repack_codes_kernel<<<blocks, threads, 0, st>>>(a, which);
+    repack_scales_kernel<<<blocks, threads, 0, st>>>(a, which);
+  }
+  repack_misc_kernel<<<blocks, threads, 0, st>>>(a);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,132 @@
+"""A thin PyTorch-facing wrapper of the C ABI: owns the device buffers (packed
+weights, alignment outputs, workspace) as torch tensors and calls the library
+in order.  It performs no arithmetic of the layer itself.
+
+Typical use::
+
+    layer = MoELayer.from_numpy(weights, device="cuda")        # repack once
+    out = layer(x, topk_ids, topk_weights)                      # align + forward
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+FMT = {"int4": B.MOE_W_INT4_U4B8, "mxfp4": B.MOE_W_MXFP4, "nvfp4": B.MOE_W_NVFP4}
+ACT = {"silu_mul": B.MOE_ACT_SILU_MUL, "sigmoid_alpha": B.MOE_ACT_SIGMOID_ALPHA}
+GROUP = {"int4": 128, "mxfp4": 32, "nvfp4": 16}
+
+
+def _dev(a: Optional[np.ndarray], device, dtype=None) -> Optional[torch.Tensor]:
+    """Host array -> device tensor with the same bytes (uint16 travels as int16)."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    t = torch.from_numpy(a)
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(device)
+
+
+@dataclasses.dataclass
+class AlignOut:
+    block_m: int
+    sorted_ids: torch.Tensor
+    expert_ids: torch.Tensor
+    n_padded: torch.Tensor
+
+
+class MoELayer:
+    """One layer's expert bank on one GPU, repacked for the kernels."""
+
+    def __init__(self, fmt: str, num_experts: int, hidden: int, inter: int, w13, w13_s, w13_gs, b13, w2, w2_s,
+                 w2_gs, b2, interleaved: bool = False, stream=None):
+        self.fmt = fmt
+        self.E, self.K, self.N = num_experts, hidden, inter
+        self.desc = B.moe_layer_desc(FMT[fmt], num_experts, hidden, inter, GROUP[fmt], int(interleaved),
+                                     int(b13 is not None), int(b2 is not None))
+        dev = w13.device
+        self.device = dev
+        self.packed = torch.empty(B.moe_repack_size(self.desc), dtype=torch.uint8, device=dev)
+        B.moe_repack_weights(self.desc, w13, w13_s, w13_gs, b13, w2, w2_s, w2_gs, b2, self.packed, stream)
+        self._ws = {}
+
+    @classmethod
+    def from_numpy(cls, W, device="cuda", stream=None) -> "MoELayer":
+        """W: a workloads.LayerWeights (host arrays in checkpoint layout)."""
+        t = dict(w13=_dev(W.w13, device), w13_s=_dev(W.w13_s, device), w13_gs=_dev(W.w13_gs, device),
+                 b13=_dev(W.b13, device), w2=_dev(W.w2, device), w2_s=_dev(W.w2_s, device),
+                 w2_gs=_dev(W.w2_gs, device), b2=_dev(W.b2, device))
+        layer = cls(W.fmt, W.E, W.K, W.N, interleaved=W.interleaved, stream=stream, **t)
+        torch.cuda.current_stream(device).synchronize()  # source tensors may be freed after this
+        return layer
+
+    # ------------------------------------------------------------ align
+    def alloc_align(self, M: int, top_k: int, block_m: int) -> AlignOut:
+        cap = B.moe_align_capacity(M, top_k, self.E, block_m)
+        d = self.device
+        return AlignOut(block_m, torch.empty(cap, dtype=torch.int32, device=d),
+                        torch.empty(max(cap // block_m, 1), dtype=torch.int32, device=d),
+                        torch.empty(1, dtype=torch.int32, device=d))
+
+    def align(self, topk_ids: torch.Tensor, expert_base: int = 0, block_m: Optional[int] = None,
+              num_routed_ids: Optional[int] = None, out: Optional[AlignOut] = None, stream=None) -> AlignOut:
+        M, k = topk_ids.shape
+        if block_m is None:
+            block_m = self.choose_block_m(M, k, num_routed_ids or self.E)
+        a = out if out is not None else self.alloc_align(M, k, block_m)
+        B.moe_align(topk_ids, M, k, expert_base, self.E, block_m, a.sorted_ids, a.expert_ids, a.n_padded, stream)
+        return a
+
+    def choose_block_m(self, M: int, top_k: int, num_routed_ids: int) -> int:
+        return B.moe_choose_block_m(self.desc, M, top_k, num_routed_ids)
+
+    # ------------------------------------------------------------ forward
+    def workspace(self, M: int, top_k: int, block_m: int) -> torch.Tensor:
+        key = (M, top_k, block_m)
+        ws = self._ws.get(key)
+        if ws is None:
+            n = B.moe_workspace_size(self.desc, M, top_k, block_m)
+            ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+            self._ws = {key: ws}  # keep one workspace alive
+        return ws
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, a: AlignOut,
+                expert_base: int = 0, act: str = "silu_mul", alpha: float = 1.702, limit: float = math.inf,
+                routed_scaling_factor: float = 1.0, post_norm_w: Optional[torch.Tensor] = None,
+                norm_eps: float = 1e-8, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+        M, k = topk_ids.shape
+        if out is None:
+            out = torch.empty((M, self.K), dtype=torch.bfloat16, device=self.device)
+        ws = workspace if workspace is not None else self.workspace(M, k, a.block_m)
+        B.moe_w4a16_forward(self.desc, self.packed, x, M, k, topk_ids, topk_weights, expert_base, a.sorted_ids,
+                            a.expert_ids, a.n_padded, a.block_m, ACT[act], alpha, limit, routed_scaling_factor,
+                            post_norm_w, norm_eps, out, ws, ws.numel(), stream)
+        return out
+
+    def __call__(self, x, topk_ids, topk_weights, expert_base: int = 0, block_m: Optional[int] = None,
+                 num_routed_ids: Optional[int] = None, **kw) -> torch.Tensor:
+        a = self.align(topk_ids, expert_base, block_m, num_routed_ids)
+        return self.forward(x, topk_ids, topk_weights, a, expert_base=expert_base, **kw)
+
+    def status(self, workspace: Optional[torch.Tensor] = None, stream=None) -> int:
+        ws = workspace if workspace is not None else next(iter(self._ws.values()))
+        return B.moe_get_status(ws, stream)
+
+
+def batch_to_device(X, device="cuda"):
+    """workloads.BatchInputs -> (x bf16, topk_ids int32, topk_weights fp32, post_norm_w bf16 or None)."""
+    x = _dev(X.x, device, torch.bfloat16)
+    ids = _dev(X.topk_ids.astype(np.int32, copy=False), device)
+    w = _dev(X.topk_weights.astype(np.float32, copy=False), device)
+    pnw = _dev(X.post_norm_w, device, torch.bfloat16)
+    return x, ids, w, pnw
