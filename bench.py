@@ -34,6 +34,10 @@ import numpy as np  # noqa: E402
 from weight_only_bit_moe_gb300 import workloads as wk  # noqa: E402
 
 DEFAULT_WORKLOAD, DEFAULT_M = "int4-bias", 2304
+SWEEP = [("int4-bias", 123), ("int4-bias", 2304), ("mxfp4-alpha", 1), ("mxfp4-alpha", 32), ("mxfp4-alpha", 1024),
+         ("nvfp4-ep-norm", 1), ("nvfp4-ep-norm", 8), ("nvfp4-ep-norm", 64), ("nvfp4-ep-norm", 512),
+         ("int4-skew", 1), ("int4-skew", 16), ("int4-skew", 256), ("int4-skew", 4096), ("int4-uniform", 16),
+         ("int4-uniform", 256), ("int4-uniform", 4096)]
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 
 
@@ -224,19 +228,23 @@ def run_ours(args, rank: int, world: int):
         clocks = clk.summary()
 
         # ---- per-kernel times: traced eager steps, queued behind a spin so launches run ahead
-        tev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        tev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
         kern = []
         for i in range(args.steps):
             flush.fill_(1)
             torch.cuda._sleep(2_000_000)
-            binding.moe_set_trace_events(tev[i])
+            t = tev[i]
+            binding.moe_set_trace_events(t[2:6])
+            t[0].record(stream)
             layer.align(ids, wl.expert_base, B, out=a)
+            t[1].record(stream)
             layer.forward(x, ids, tw, a, **kw)
             binding.moe_set_trace_events(None)
         stream.synchronize()
         for i in range(args.steps):
             t = tev[i]
-            kern.append((t[0].elapsed_time(t[1]), t[1].elapsed_time(t[2]), t[2].elapsed_time(t[3])))
+            kern.append((t[2].elapsed_time(t[3]), t[3].elapsed_time(t[4]), t[4].elapsed_time(t[5]),
+                         t[0].elapsed_time(t[1])))
         if layer.status() != 0:
             raise RuntimeError("device status not ok after the timed steps")
 
@@ -277,6 +285,7 @@ def run_ours(args, rank: int, world: int):
     g1 = statistics.mean(k[0] for k in kern)
     g2 = statistics.mean(k[1] for k in kern)
     cb = statistics.mean(k[2] for k in kern)
+    al = statistics.mean(k[3] for k in kern)
     hbm, tc_burst, tc_sus, src = peaks()
     t_hbm = alg["bytes"] / (hbm * 1e9)
     t_tc = alg["flops"] / (tc_burst * 1e12)
@@ -296,7 +305,7 @@ def run_ours(args, rank: int, world: int):
                  "kernel_ms": round(dom_ms, 5)})
 
     # ---- CPU oracle on a bounded sample of the same batch
-    cpu = cpu_baseline(wl, W, X, budget_s=args.cpu_budget)
+    cpu = cpu_baseline(wl, W, X, budget_s=args.cpu_budget) if args.cpu_budget > 0 else None
 
     value = world * M / (ms * 1e-3)
     line = {
@@ -313,10 +322,11 @@ def run_ours(args, rank: int, world: int):
                           "t_roof_us": round(max(t_hbm, t_tc) * 1e6, 3),
                           "frac_of_step": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
                           "bound": "tensor" if tensor_bound else "hbm"},
-        "kernels_ms": {"gemm1": round(g1, 5), "gemm2": round(g2, 5), "combine": round(cb, 5)},
+        "kernels_ms": {"align": round(al, 5), "gemm1": round(g1, 5), "gemm2": round(g2, 5),
+                       "combine": round(cb, 5)},
         "e2e": {"value": round(world * M / (e2e * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e, 4)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -384,8 +394,18 @@ def main():
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--sweep", action="store_true",
+                    help="one line per workload shape of the parity suite (analysis; not the headline line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep:
+        import torch
+        for name, M in SWEEP:
+            args.workload, args.M = name, M
+            line = run_ours(args, 0, 1)
+            print(json.dumps(line), flush=True)
+            torch.cuda.empty_cache()
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -150,7 +150,11 @@ int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int blo
  * sorted_ids / expert_ids / n_padded from moe_align with the same M, top_k,
  * expert_base, E and block_m; act a moe_act; alpha, limit (host) for
  * SIGMOID_ALPHA (limit = +inf: no clamp); post_norm_w bf16 [K] or NULL;
- * out bf16 [M, K]; workspace of at least moe_workspace_size() bytes.
+ * out bf16 [M, K]; workspace of at least moe_workspace_size() bytes.  packed and
+ * workspace must be 256-byte aligned; x, out and post_norm_w 16-byte aligned.
+ * Operand range: the tensor-core operands are 16-bit (fp16 for GEMM2 and for
+ * INT4's GEMM1), so inputs and activations must stay inside the fp16 range
+ * (|v| < 65504); MXFP4 scales must lie in [2^-20, 2^9] (E8M0 bytes 107..136).
  * M == 0 is a no-op. */
 int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void* x, int M,
                       int top_k, const int32_t* topk_ids, const float* topk_weights,

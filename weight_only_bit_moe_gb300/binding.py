@@ -40,9 +40,11 @@ _lib = None
 _lock = threading.Lock()
 
 
-def load(path: str = LIB_PATH):
-    """Load the CUDA library (once).  Raises if it is missing: there is no fallback."""
+def load(path: str = ""):
+    """Load the CUDA library (once).  Raises if it is missing: there is no fallback.
+    MOE_W4A16_LIB overrides the library path (e.g. an alternative build)."""
     global _lib
+    path = path or os.environ.get("MOE_W4A16_LIB", LIB_PATH)
     with _lock:
         if _lib is None:
             if not os.path.exists(path):

@@ -5,13 +5,15 @@
 // (sglang PR #31552), marlin_template.h).
 //
 // One CTA of 1024 threads does the whole job, which at the layer's sizes
-// (<= 32768 pairs) costs a few microseconds:
-//   1. histogram of local expert ids in shared memory;
-//   2. padded counts -> exclusive scan -> run starts, n_padded, block experts;
-//   3. stable scatter, 1024 pairs per round: each warp's __match_any_sync mask
-//      is the 32-bit membership word of its expert; one warp per expert scans
-//      the 32 words of a round, which gives every pair its rank among earlier
-//      pairs of the same expert without atomics, so ties keep pair order.
+// (<= 32768 pairs) costs a few microseconds.  It is a stable counting sort:
+//   1. each of the 32 warps owns a contiguous segment of pairs and counts its
+//      segment's local expert ids into its own row of a [32][E] table;
+//   2. per expert, the segment counts give the total; the padded totals are
+//      scanned into run starts, n_padded and the block -> expert table;
+//   3. per expert, the table is turned into exclusive offsets across warps;
+//   4. each warp walks its segment in order, 32 pairs at a time: the lanes that
+//      share an expert (__match_any_sync) take consecutive slots after that
+//      expert's running offset, so equal experts keep ascending pair order.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,7 +22,14 @@
 namespace moe {
 
 constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kAlignMaxExperts = 1024;
+constexpr int kAlignBatch = 16;  // rounds of 32 ids a warp loads at once
+
+__device__ __forceinline__ int local_expert(const int32_t* ids, int p, int base, int E) {
+  const int e = ids[p] - base;
+  return (e >= 0 && e < E) ? e : -1;
+}
 
 __global__ void __launch_bounds__(kAlignThreads, 1)
     align_kernel(const int32_t* __restrict__ topk_ids, int pairs, int expert_base, int num_experts, int block_m,
@@ -28,28 +37,43 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
                  int32_t* __restrict__ n_padded) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int E = num_experts;
-  uint32_t* words = reinterpret_cast<uint32_t*>(smem);           // [E][32] membership words
-  uint16_t* prefix = reinterpret_cast<uint16_t*>(words + E * 32);  // [E][32] exclusive ranks
-  int* count = reinterpret_cast<int*>(prefix + E * 32);           // [E]
-  int* start = count + E;                                         // [E]
-  int* run = start + E;                                           // [E] pairs placed so far
-  int* tot = run + E;                                             // [E] pairs in this round
+  int* tab = reinterpret_cast<int*>(smem);  // [32][E] segment counts, then segment offsets
+  int* count = tab + kAlignWarps * E;       // [E]
+  int* start = count + E;                   // [E]
   __shared__ int warp_sums[32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < E * 32; i += kAlignThreads) words[i] = 0u;
-  for (int e = tid; e < E; e += kAlignThreads) { count[e] = 0; run[e] = 0; }
-  __syncthreads();
+  const int seg = (pairs + kAlignWarps - 1) / kAlignWarps;
+  const int p0 = warp * seg, p1 = min(pairs, p0 + seg);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int* row = tab + warp * E;
 
-  // 1. histogram
-  for (int p = tid; p < pairs; p += kAlignThreads) {
-    const int e = topk_ids[p] - expert_base;
-    if (e >= 0 && e < E) atomicAdd(&count[e], 1);
+  // 1. segment counts; a warp loads up to 32 rounds of ids at once (one round
+  //    trip), then counts them
+  for (int e = lane; e < E; e += 32) row[e] = 0;
+  __syncwarp();
+  for (int pass = p0; pass < p1; pass += 32 * kAlignBatch) {
+    int ev[kAlignBatch];
+#pragma unroll
+    for (int i = 0; i < kAlignBatch; ++i) {
+      const int p = pass + 32 * i + lane;
+      ev[i] = p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kAlignBatch; ++i) {
+      if (pass + 32 * i >= p1) break;
+      const uint32_t m = __match_any_sync(0xffffffffu, ev[i]);
+      if (ev[i] >= 0 && (m & lt_mask) == 0) row[ev[i]] += __popc(m);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
-  // 2. exclusive scan of padded counts (E <= 1024: one value per thread)
-  const int padded = tid < E ? (count[tid] + block_m - 1) / block_m * block_m : 0;
+  // 2. totals, padded scan (E <= 1024: one expert per thread)
+  int c = 0;
+  if (tid < E)
+    for (int w = 0; w < kAlignWarps; ++w) c += tab[w * E + tid];
+  const int padded = (c + block_m - 1) / block_m * block_m;
   int incl = padded;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -59,62 +83,60 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int s = warp_sums[lane];
+    int sum = warp_sums[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += v;
+      const int v = __shfl_up_sync(0xffffffffu, sum, o);
+      if (lane >= o) sum += v;
     }
-    warp_sums[lane] = s;  // inclusive over warps
+    warp_sums[lane] = sum;  // inclusive over warps
   }
   __syncthreads();
   const int total = warp_sums[31];
-  if (tid < E) start[tid] = incl - padded + (warp ? warp_sums[warp - 1] : 0);
+  if (tid < E) {
+    const int s0 = incl - padded + (warp ? warp_sums[warp - 1] : 0);
+    count[tid] = c;
+    start[tid] = s0;
+    // 3. exclusive offsets of each segment within the expert's run
+    int run = s0;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int v = tab[w * E + tid];
+      tab[w * E + tid] = run;
+      run += v;
+    }
+  }
   if (tid == 0) *n_padded = total;
   __syncthreads();
 
   // block experts, padding sentinels, tail
   const int32_t sentinel = pairs;
   for (int e = tid; e < E; e += kAlignThreads) {
-    const int s0 = start[e], c = count[e];
-    const int pe = (c + block_m - 1) / block_m * block_m;
+    const int s0 = start[e], ce = count[e];
+    const int pe = (ce + block_m - 1) / block_m * block_m;
     for (int b = s0 / block_m; b < (s0 + pe) / block_m; ++b) expert_ids[b] = e;
-    for (int i = c; i < pe; ++i) sorted_ids[s0 + i] = sentinel;
+    for (int i = ce; i < pe; ++i) sorted_ids[s0 + i] = sentinel;
   }
   for (int64_t i = total + tid; i < cap; i += kAlignThreads) sorted_ids[i] = sentinel;
   for (int64_t b = total / block_m + tid; b < cap / block_m; b += kAlignThreads) expert_ids[b] = -1;
 
-  // 3. stable scatter, one round of 1024 pairs at a time
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < pairs; base += kAlignThreads) {
-    const int p = base + tid;
-    int e = -1;
-    if (p < pairs) {
-      e = topk_ids[p] - expert_base;
-      if (e < 0 || e >= E) e = -1;
-    }
-    const uint32_t m = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && (m & lt_mask) == 0) words[e * 32 + warp] = m;  // group leader
-    __syncthreads();
-    // one warp per expert: exclusive prefix of popcounts over the 32 warps
-    for (int ex = warp; ex < E; ex += 32) {
-      const uint32_t w = words[ex * 32 + lane];
-      const int c = __popc(w);
-      int s = c;
+  // 4. stable scatter of each segment, rounds in pair order
+  for (int pass = p0; pass < p1; pass += 32 * kAlignBatch) {
+    int ev[kAlignBatch];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += v;
-      }
-      prefix[ex * 32 + lane] = (uint16_t)(s - c);
-      words[ex * 32 + lane] = 0u;
-      if (lane == 31) tot[ex] = s;
+    for (int i = 0; i < kAlignBatch; ++i) {
+      const int p = pass + 32 * i + lane;
+      ev[i] = p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1;
     }
-    __syncthreads();
-    if (e >= 0) sorted_ids[start[e] + run[e] + prefix[e * 32 + warp] + __popc(m & lt_mask)] = p;
-    __syncthreads();
-    for (int ex = tid; ex < E; ex += kAlignThreads) run[ex] += tot[ex];
-    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kAlignBatch; ++i) {
+      if (pass + 32 * i >= p1) break;
+      const int e = ev[i];
+      const uint32_t m = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) sorted_ids[row[e] + __popc(m & lt_mask)] = pass + 32 * i + lane;
+      __syncwarp();
+      if (e >= 0 && (m & lt_mask) == 0) row[e] += __popc(m);
+      __syncwarp();
+    }
   }
 }
 
@@ -138,13 +160,15 @@ extern "C" int moe_align(const int32_t* topk_ids, int M, int top_k, int expert_b
   if ((int64_t)M * top_k >= (int64_t)1 << 31) return MOE_ERR_INVALID;
   if (!sorted_ids || !expert_ids || !n_padded || (M > 0 && !topk_ids)) return MOE_ERR_INVALID;
   const int64_t cap = moe_align_capacity(M, top_k, num_experts, block_m);
-  const size_t smem = (size_t)num_experts * 32 * (4 + 2) + (size_t)num_experts * 4 * 4;
-  static bool attr_set = false;
-  if (!attr_set) {
+  const size_t smem = ((size_t)kAlignWarps + 2) * num_experts * 4;
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!configured[dev]) {
     if (cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)kAlignMaxExperts * 32 * 6 + kAlignMaxExperts * 16)) != cudaSuccess)
+                             (int)(((size_t)kAlignWarps + 2) * kAlignMaxExperts * 4)) != cudaSuccess)
       return MOE_ERR_CUDA;
-    attr_set = true;
+    configured[dev] = true;
   }
   align_kernel<<<1, kAlignThreads, smem, (cudaStream_t)stream>>>(topk_ids, M * top_k, expert_base, num_experts,
                                                                  block_m, cap, sorted_ids, expert_ids, n_padded);

@@ -1,12 +1,15 @@
 // Host side of the C ABI: argument checks, the launch-configuration chooser,
 // the workspace plan and the forward's launch sequence (GEMM1 + activation ->
 // GEMM2 -> combine), all enqueued on the caller's stream without host syncs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "combine.cuh"
 #include "gemm_launch.cuh"
+#include "prep.cuh"
 
 namespace moe {
 
@@ -30,7 +33,8 @@ struct WsPlan {
   int64_t cap, blocks;
   int grid;
   int max_split1, max_split2, rows1, rows2;
-  int64_t status_off, counters_off, counters_bytes, a_off, y_off, inv_off, part1_off, part2_off, total;
+  int64_t status_off, counters1_off, counters2_off, header_bytes, xs_off, a_off, y_off, part1_off, part2_off,
+      total;
 };
 
 bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w) {
@@ -51,15 +55,18 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w) {
   int64_t off = 0;
   w->status_off = off;
   off += 256;
-  w->counters_off = off;
-  w->counters_bytes = (int64_t)L.T1 * w->blocks * 4;
-  off = round_up64(off + w->counters_bytes, 256);
+  w->counters1_off = off;
+  off += (int64_t)L.T1 * w->blocks * 4;
+  w->counters2_off = off;
+  off += (int64_t)L.T2 * w->blocks * 4;
+  w->header_bytes = off;  // zeroed by the prologue every call
+  off = round_up64(off, 256);
+  w->xs_off = off;  // routed rows in sorted order, 16-bit
+  off = round_up64(off + cap * L.K * 2, 256);
   w->a_off = off;
   off = round_up64(off + cap * L.Npad * 2, 256);
   w->y_off = off;
   off = round_up64(off + pairs * L.K * 4, 256);
-  w->inv_off = off;
-  off = round_up64(off + pairs * 4, 256);
   w->part1_off = off;
   off = round_up64(off + (int64_t)w->max_split1 * per1, 256);
   w->part2_off = off;
@@ -78,6 +85,34 @@ cudaError_t launch_gemm(int fmt, bool gated, int bn, const GemmArgs& g, int grid
 }
 
 bool valid_block_m(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major [rows, cols] 16-bit matrix, 128-byte swizzled boxes of box_rows x 64.
+bool make_act_map(CUtensorMap* m, const void* base, bool f16, int64_t cols, int64_t rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1u, 1u};
+  return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 cudaEvent_t g_trace[4] = {nullptr, nullptr, nullptr, nullptr};
 bool g_tracing = false;
@@ -124,7 +159,8 @@ extern "C" int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed,
       !workspace)
     return MOE_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(packed) & 255) || (reinterpret_cast<uintptr_t>(workspace) & 255) ||
-      (reinterpret_cast<uintptr_t>(x) & 15))
+      (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
+      (reinterpret_cast<uintptr_t>(post_norm_w) & 15))
     return MOE_ERR_INVALID;
   WsPlan w;
   if (!plan_workspace(L, M, top_k, block_m, &w)) return MOE_ERR_CUDA;
@@ -134,46 +170,58 @@ extern "C" int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed,
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   const int bn = block_m < 16 ? 16 : block_m;
 
-  // status word, chosen split and split-K arrival counters start at zero every call
-  if (cudaMemsetAsync(ws, 0, w.counters_off + w.counters_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  GemmArgs g{};
+  // GEMM1 reads the gathered fp16 rows; GEMM2 GEMM1's fp16 output
+  if (!make_act_map(&g.tmap_b, ws + w.xs_off, true, L.K, w.cap, bn)) return MOE_ERR_CUDA;
+  CUtensorMap map2;
+  if (!make_act_map(&map2, ws + w.a_off, true, L.Npad, w.cap, bn)) return MOE_ERR_CUDA;
+
+  // prologue: status word and split-K counters to zero, routed rows gathered
+  PrepArgs pa{};
+  pa.zero = reinterpret_cast<uint32_t*>(ws);
+  pa.zero_words = w.header_bytes / 4;
+  pa.x = static_cast<const uint16_t*>(x);
+  pa.xs = reinterpret_cast<uint16_t*>(ws + w.xs_off);
+  pa.sorted_ids = sorted_ids;
+  pa.n_padded = n_padded;
+  pa.cap = w.cap;
+  pa.pairs = M * top_k;
+  pa.top_k = top_k;
+  pa.K = L.K;
+  pa.to_f16 = 1;
+  if (launch_prep(pa, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(0, st) != cudaSuccess) return MOE_ERR_CUDA;
 
-  GemmArgs g{};
   g.L = L;
   g.packed = pk;
   g.sorted_ids = sorted_ids;
   g.expert_ids = expert_ids;
   g.n_padded = n_padded;
   g.pairs = M * top_k;
-  g.top_k = top_k;
   g.block_m = block_m;
   g.act_kind = act;
   g.alpha = alpha;
   g.limit = limit;
   g.a_out = reinterpret_cast<uint16_t*>(ws + w.a_off);
   g.y_out = reinterpret_cast<float*>(ws + w.y_off);
-  g.inv_pos = reinterpret_cast<int32_t*>(ws + w.inv_off);
-  g.counters = reinterpret_cast<int32_t*>(ws + w.counters_off);
-  g.split_used = reinterpret_cast<int32_t*>(ws + w.status_off + 4);
   g.status = reinterpret_cast<unsigned*>(ws + w.status_off);
 
   // GEMM1 + activation
-  g.act = static_cast<const uint16_t*>(x);
-  g.act_ld = L.K;
   g.has_bias = desc->has_bias13 != 0;
   g.max_split = w.max_split1;
   g.split_rows = w.rows1;
   g.partial = reinterpret_cast<float*>(ws + w.part1_off);
+  g.counters = reinterpret_cast<int32_t*>(ws + w.counters1_off);
   if (launch_gemm(L.fmt, true, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(1, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2
-  g.act = g.a_out;
-  g.act_ld = L.Npad;
+  g.tmap_b = map2;
   g.has_bias = desc->has_bias2 != 0;
   g.max_split = w.max_split2;
   g.split_rows = w.rows2;
   g.partial = reinterpret_cast<float*>(ws + w.part2_off);
+  g.counters = reinterpret_cast<int32_t*>(ws + w.counters2_off);
   if (launch_gemm(L.fmt, false, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(2, st) != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -182,18 +230,11 @@ extern "C" int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed,
   c.M = M;
   c.top_k = top_k;
   c.K = L.K;
-  c.Kpad2 = L.Kpad2;
   c.expert_base = expert_base;
   c.E = L.E;
   c.topk_ids = topk_ids;
   c.topk_weights = topk_weights;
   c.y = reinterpret_cast<const float*>(ws + w.y_off);
-  c.partial = reinterpret_cast<const float*>(ws + w.part2_off);
-  c.split_rows = w.rows2;
-  c.split_used = g.split_used;
-  c.inv_pos = g.inv_pos;
-  c.gs2 = reinterpret_cast<const float*>(pk + L.gs2_off);
-  c.b2 = desc->has_bias2 ? reinterpret_cast<const uint16_t*>(pk + L.b2_off) : nullptr;
   c.post_norm_w = static_cast<const uint16_t*>(post_norm_w);
   c.norm_eps = norm_eps;
   c.rsf = routed_scaling_factor;

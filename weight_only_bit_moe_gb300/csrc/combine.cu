@@ -10,9 +10,10 @@
 //              _expert_norm_sum, weight_first, eps 1e-8; non-local slots get
 //              factor 0).
 //
-// One CTA per token; y is fp32.  When GEMM2 ran split-K the combine also
-// finishes GEMM2: it sums the fp32 partial slices in split order and applies the
-// global scale and bias -- what GEMM2's own epilogue does otherwise.
+// y is fp32.  Each thread owns 8 consecutive columns (two 16-byte loads per
+// slot, one 16-byte bf16 store) and issues every slot's loads before it sums,
+// in slot order.  The plain combine spreads a token over a 2-D grid of column
+// chunks; the post-norm combine keeps one CTA per token for its row reduction.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,79 +21,146 @@
 
 namespace moe {
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 128;
+constexpr int kCols = 8;  // columns per thread
 constexpr int kMaxTopK = 16;
 
-__device__ __forceinline__ float pair_y(const CombineArgs& c, int split, int pair, int e, int col) {
-  if (split == 1) return c.y[(int64_t)pair * c.K + col];
-  const int pos = c.inv_pos[pair];
-  float acc = 0.f;
-  for (int s = 0; s < split; ++s) acc += __ldcg(c.partial + ((int64_t)s * c.split_rows + pos) * c.K + col);
-  const float b = c.b2 ? bf16_bits_to_float(c.b2[(int64_t)e * c.Kpad2 + col]) : 0.f;
-  return acc * c.gs2[e] + b;
+__device__ __forceinline__ void ld8(const float* p, float (&v)[8]) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void bf16x8(const uint16_t* p, float (&v)[8]) {  // 8 bf16 -> fp32
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// y of one pair at columns [col, col+8).
+__device__ __forceinline__ void pair_y8(const CombineArgs& c, int pair, int col, float (&v)[8]) {
+  ld8(c.y + (int64_t)pair * c.K + col, v);
+}
+
+__device__ __forceinline__ void norm_w8(const uint16_t* w, int col, float (&v)[8]) {
+  bf16x8(w + col, v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = round_bf16(1.0f + v[i]);  // bf16(fp32(1 + w))
+}
+
+__device__ __forceinline__ void store8(uint16_t* out, const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = (uint32_t)float_to_bf16_bits(v[2 * i]) | ((uint32_t)float_to_bf16_bits(v[2 * i + 1]) << 16);
+  *reinterpret_cast<uint4*>(out) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineArgs c) {
-  __shared__ int s_e[kMaxTopK];
-  __shared__ float s_w[kMaxTopK];
-  __shared__ float s_red[kCombineThreads / 32][kMaxTopK];
-  __shared__ float s_inv[kMaxTopK];
   const int t = blockIdx.x, tid = threadIdx.x;
   const int k = c.top_k;
-  if (tid < k) {
-    const int e = c.topk_ids[(int64_t)t * k + tid] - c.expert_base;
-    s_e[tid] = (e >= 0 && e < c.E) ? e : -1;
-    s_w[tid] = c.topk_weights[(int64_t)t * k + tid];
-  }
-  __syncthreads();
-  const int split = *c.split_used;
-  if (c.post_norm_w) {
-    float ss[kMaxTopK];
+  int e[kMaxTopK];
+  float w[kMaxTopK];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) ss[j] = 0.f;
-    for (int col = tid; col < c.K; col += kCombineThreads) {
-      const float nw = round_bf16(1.0f + bf16_bits_to_float(c.post_norm_w[col]));
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        if (j < k && s_e[j] >= 0) {
-          const float z = pair_y(c, split, t * k + j, s_e[j], col) * nw;
-          ss[j] += z * z;
-        }
+  for (int j = 0; j < kMaxTopK; ++j) {
+    e[j] = -1;
+    w[j] = 0.f;
+    if (j < k) {
+      const int ej = c.topk_ids[(int64_t)t * k + j] - c.expert_base;
+      if (ej >= 0 && ej < c.E) {
+        e[j] = ej;
+        w[j] = c.topk_weights[(int64_t)t * k + j];
       }
     }
-    const int lane = tid & 31, warp = tid >> 5;
+  }
+  uint16_t* orow = c.out + (int64_t)t * c.K;
+
+  if (!c.post_norm_w) {
+    const int col = (blockIdx.y * kCombineThreads + tid) * kCols;
+    if (col >= c.K) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
-      float v = ss[j];
+      if (j >= k) break;
+      if (e[j] < 0) continue;
+      float y[8];
+      pair_y8(c, t * k + j, col, y);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) s_red[warp][j] = v;
+      for (int i = 0; i < 8; ++i) acc[i] += w[j] * y[i];
     }
-    __syncthreads();
-    if (tid < k) {
-      float v = 0.f;
-      for (int w = 0; w < kCombineThreads / 32; ++w) v += s_red[w][tid];
-      s_inv[tid] = 1.0f / sqrtf(v / (float)c.K + c.norm_eps);
-    }
-    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= c.rsf;
+    store8(orow + col, acc);
+    return;
   }
-  for (int col = tid; col < c.K; col += kCombineThreads) {
-    const float nw = c.post_norm_w ? round_bf16(1.0f + bf16_bits_to_float(c.post_norm_w[col])) : 1.0f;
-    float acc = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int e = s_e[j];
-      if (e < 0) continue;
-      const float y = pair_y(c, split, t * k + j, e, col);
-      acc += c.post_norm_w ? s_w[j] * s_inv[j] * (y * nw) : s_w[j] * y;
+
+  // post-expert norm: per-slot sum of squares over the whole row first
+  __shared__ float s_red[kCombineThreads / 32][kMaxTopK];
+  __shared__ float s_inv[kMaxTopK];
+  float ss[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) ss[j] = 0.f;
+  for (int col = tid * kCols; col < c.K; col += kCombineThreads * kCols) {
+    float nw[8];
+    norm_w8(c.post_norm_w, col, nw);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      if (e[j] < 0) continue;
+      float y[8];
+      pair_y8(c, t * k + j, col, y);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float z = y[i] * nw[i];
+        ss[j] += z * z;
+      }
     }
-    c.out[(int64_t)t * c.K + col] = float_to_bf16_bits(c.rsf * acc);
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    float v = ss[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_red[warp][j] = v;
+  }
+  __syncthreads();
+  if (tid < kMaxTopK) {
+    float v = 0.f;
+    for (int i = 0; i < kCombineThreads / 32; ++i) v += s_red[i][tid];
+    s_inv[tid] = 1.0f / sqrtf(v / (float)c.K + c.norm_eps);
+  }
+  __syncthreads();
+  for (int col = tid * kCols; col < c.K; col += kCombineThreads * kCols) {
+    float nw[8];
+    norm_w8(c.post_norm_w, col, nw);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      if (e[j] < 0) continue;
+      float y[8];
+      pair_y8(c, t * k + j, col, y);
+      const float f = w[j] * s_inv[j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f * (y[i] * nw[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= c.rsf;
+    store8(orow + col, acc);
   }
 }
 
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t st) {
   if (c.M == 0) return cudaSuccess;
-  if (c.top_k > kMaxTopK) return cudaErrorInvalidValue;
-  combine_kernel<<<c.M, kCombineThreads, 0, st>>>(c);
+  if (c.top_k > kMaxTopK || c.K % kCols) return cudaErrorInvalidValue;
+  const int chunks = (c.K / kCols + kCombineThreads - 1) / kCombineThreads;
+  const dim3 grid(c.M, c.post_norm_w ? 1 : chunks);
+  combine_kernel<<<grid, kCombineThreads, 0, st>>>(c);
   return cudaPeekAtLastError();
 }
 

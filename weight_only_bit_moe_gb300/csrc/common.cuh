@@ -26,8 +26,9 @@ namespace moe {
 // packed codes are 8 KiB: uint4 units [j][r] (j = 0,1 is the 32-element half of
 // the stage, r the tile row), so that thread r of the dequant warps reads
 // units r and 256 + r, both conflict-free.  Inside one 32-bit word (8 elements
-// e0..e7 of a row), element 2i sits at bits 4i and element 2i+1 at bits 16+4i:
-// one shift and mask yields a bf16x2 pair of consecutive elements.
+// e0..e7 of a row): INT4 puts element 2i at bits 4i and element 2i+1 at bits
+// 16+4i (a mask yields an f16x2 pair of consecutive elements); FP4 keeps element
+// order, two codes per byte, for the hardware E2M1x2 -> f16x2 conversion.
 //
 // Scales ride in front of the stage that first needs them: INT4 (one bf16 per
 // 128 = two stages) only in front of even stages, 256 x bf16; MXFP4 two E8M0
@@ -136,14 +137,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+// Test the phase with the given parity; while it is incomplete the thread is
+// suspended (it issues nothing) until the phase completes or the hint (ns)
+// elapses, so waiting roles do not steal issue slots from working warps.
+constexpr uint32_t kSuspendHintNs = 1000000u;  // 1 ms
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -156,16 +161,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicOr(status, kStatusTimeout);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
     }
   }
 }
@@ -246,6 +249,46 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T: A is read from tensor memory, one row per
+// lane, two 16-bit K elements per 32-bit column (8 columns per K=16 step).
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+// 32 TMEM lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // 32 TMEM lanes x 16 consecutive 32-bit columns; lane = warp quarter + thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -304,72 +347,76 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 __device__ __forceinline__ float round_bf16(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
 
 // ---------------------------------------------------------------- dequant
-// Per-stage scale multipliers of one row, as bf16x2 (same value in both lanes).
-// INT4: the bf16 scale itself.  FP4: the block scale times 2^118 (E2M1 codes are
-// decoded as bf16 patterns that stand for value * 2^-126, see below; the product
-// is then value * scale * 2^-8, undone in the epilogue by kFp4Unscale).
-__device__ __forceinline__ uint32_t e8m0_mult_bits(uint32_t b) {
-  // 2^(b-127) * 2^118 = 2^(b-9): bf16 exponent field b - 9 + 127 = b + 118
-  return ((b + 118u) & 0xFFu) << 7;
-}
-__device__ __forceinline__ uint32_t e4m3_mult_bits(uint32_t b) {
-  // value(b) * 2^118 computed in fp32 (exact), then as bf16 (exact: 4 significant bits)
-  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
-  float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;  // m/8 * 2^-6
-  v *= 3.3230699894622794e35f;  // 2^118
-  return (__float_as_uint(v) >> 16) & 0x7FFFu;
+// All tensor-core operands are fp16.  Every dequantised weight is exact in fp16:
+// INT4 (q - 8) * s has at most 3 + 8 significant bits; E2M1 times a power of two
+// (MXFP4) or times an E4M3 value (NVFP4) at most 2 + 4.  FP4 weights are
+// produced as value * scale * 2^-8 (kFp4Unscale restores the 2^8 in the fp32
+// epilogue), which keeps large block scales inside the fp16 range.
+
+// 8 INT4 (uint4b8) codes of one word -> 4 f16x2, elements in order.  Word
+// layout from the repack: element 2i at bits 4i, element 2i+1 at bits 16 + 4i.
+// Pairs 0 and 2 are (1024 + q) - 1032; pairs 1 and 3 sit 4 bits higher and
+// are (1024 + 16q) - 1152 = 16(q - 8), scaled by s / 16.
+__device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t s2, uint32_t s2_16, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t t[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x64006400u,
+                         (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x64006400u};
+  const __half2 c1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 c1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 sa = *reinterpret_cast<const __half2*>(&s2), sb = *reinterpret_cast<const __half2*>(&s2_16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t[i]), (i & 1) ? c1152 : c1032);
+    const __half2 r = __hmul2(v, (i & 1) ? sb : sa);
+    o[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
 }
 
-// ---- fp16 operands (every format): exact for all three, since (q - 8) * s has
-// at most 11 significant bits and E2M1 x scale at most 6.
-// INT4 (uint4b8): pair i of word w -> f16x2 (q - 8) * s, s the scale as fp16.
-__device__ __forceinline__ uint32_t dq_int4_pair_f16(uint32_t w, int i, uint32_t s2) {
-  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;  // 1024 + q, exact
-  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
-  const __half2 r = __hmul2(v, *reinterpret_cast<const __half2*>(&s2));
-  return *reinterpret_cast<const uint32_t*>(&r);
+// 8 E2M1 codes of one word (byte i = element 2i low nibble, 2i+1 high nibble)
+// -> 4 f16x2 with the hardware conversion, each times its multiplier pair.
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t m01, uint32_t m23, uint32_t (&o)[4]) {
+  uint32_t v[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+      : "r"(w));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t m = i < 2 ? m01 : m23;
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&v[i]), *reinterpret_cast<const __half2*>(&m));
+    o[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
 }
-// E2M1: sign -> bit 15, exponent/mantissa -> bits 11..9 of the fp16 pattern,
-// i.e. the pattern of value * 2^-14 (0.5 is an fp16 subnormal, exact), times
-// the multiplier scale * 2^6, giving value * scale * 2^-8.
-__device__ __forceinline__ uint32_t dq_e2m1_pair_f16(uint32_t w, int i, uint32_t m2) {
-  const uint32_t t = w >> (4 * i);
-  const uint32_t p = ((t << 9) & 0x0E000E00u) | ((t << 12) & 0x80008000u);
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&p), *reinterpret_cast<const __half2*>(&m2));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-__device__ __forceinline__ uint32_t e8m0_mult_f16(uint32_t b) {
-  // 2^(b-127) * 2^6 = 2^(b-121): fp16 exponent field b - 106 (b in [107, 136])
-  return ((b - 106u) & 0x1Fu) << 10;
-}
-__device__ __forceinline__ uint32_t e4m3_mult_f16(uint32_t b) {
-  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
-  float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
-  return __half_as_ushort(__float2half_rn(v * 64.0f));
-}
+
+// Multipliers (as f16 bit patterns, to be paired by the caller).
 __device__ __forceinline__ uint32_t bf16_scale_f16(uint32_t sbits) {
   return __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
+}
+// E8M0 byte b -> 2^(b-127) * 2^-8 = 2^(b-135) as fp16 (normal for b >= 121,
+// subnormal power of two for 111 <= b <= 120).
+__device__ __forceinline__ uint32_t e8m0_mult_f16(uint32_t b) {
+  return b >= 121u ? (((b - 120u) & 0x1Fu) << 10) : (b >= 111u ? (1u << (b - 111u)) : 0u);
+}
+// Two E4M3 bytes (low = first) -> f16x2 of value * 2^-8 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_mult_f16(uint32_t two_bytes) {
+  uint32_t v;
+  asm("{\n\t.reg .b16 h;\n\t"
+      "cvt.u16.u32 h, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h;\n\t}"
+      : "=r"(v)
+      : "r"(two_bytes));
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&v),
+                            __halves2half2(__ushort_as_half(0x1C00), __ushort_as_half(0x1C00)));  // 2^-8
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 // 8 bf16 -> 8 fp16 (round to nearest; exact inside the fp16 range).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
   const __half2 h = __floats2half2_rn(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// ---- bf16 operands (FP4 formats in GEMM1, whose B operand is the bf16 input).
-// INT4 (uint4b8): pair i of word w -> bf16x2 (q - 8) * s.
-__device__ __forceinline__ uint32_t dq_int4_pair(uint32_t w, int i, uint32_t s2) {
-  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;  // 128 + q, exact
-  const __nv_bfloat162 v = __hsub2(bits_bf162(t), bits_bf162(0x43084308u));  // - 136 -> q - 8, exact
-  return bf162_bits(__hmul2(v, bits_bf162(s2)));
-}
-// E2M1: sign -> bit 15, exponent/mantissa -> bits 8..6 of the bf16 pattern,
-// i.e. the pattern of value * 2^-126 (E2M1's subnormal 0.5 maps to a bf16
-// subnormal, exact), then times the multiplier.
-__device__ __forceinline__ uint32_t dq_e2m1_pair(uint32_t w, int i, uint32_t m2) {
-  const uint32_t t = w >> (4 * i);
-  const uint32_t p = ((t << 6) & 0x01C001C0u) | ((t << 12) & 0x80008000u);
-  return bf162_bits(__hmul2(bits_bf162(p), bits_bf162(m2)));
 }
 
 }  // namespace moe

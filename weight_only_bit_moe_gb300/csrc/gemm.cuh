@@ -10,52 +10,59 @@
 //   * swap-AB: weights are the MMA's M side (two 128-row halves per tile),
 //     routed tokens of one aligned block are the N side (16..128), so decode
 //     sizes still fill the 128-lane tensor-core tile;
-//   * a persistent grid (one CTA per SM) walks work items (tile, block, K-split)
-//     derived on the device from n_padded, splitting K when there are too few
-//     items to fill the GPU (decode) and reducing the fp32 partials in fixed
-//     split order (bitwise reproducible; the last CTA to arrive on a per-item
-//     counter does the reduction, no spinning);
-//   * operands: GEMM2 and the INT4 GEMM1 run fp16 x fp16 (every dequantised
-//     weight is exact in fp16, and the activation operand keeps 11 significant
-//     bits); the FP4 GEMM1 runs bf16 x bf16 on the bf16 input as is (E2M1 times
-//     its scale is exact in bf16).  For the INT4 GEMM1 the dequant warps convert
-//     the staged bf16 input rows to fp16 in shared memory.  Accumulation, bias,
-//     scales and the activation are fp32; only the tensor-core operands are 16-bit;
-//   * warp roles: a TMA producer streams each stage's packed codes + scales
-//     (one contiguous chunk thanks to the repack) with 1-D bulk copies; a loader
-//     warp gathers the block's activation rows with cp.async; eight dequant
-//     warps turn 4-bit codes into bf16 in registers and write the 128-byte
-//     swizzled K-major operand; one thread issues tcgen05.mma into a
-//     double-buffered TMEM accumulator; four epilogue warps read TMEM, add bias,
-//     scale, round to bf16 and apply the activation (GEMM1) or scatter rows to
-//     their pairs (GEMM2) while the next item's MMAs run.
+//   * the dequantised weights never touch shared memory: eight dequant warps
+//     (each thread one row of a 64-element stage) turn 4-bit codes into fp16 in
+//     registers -- E2M1 through the hardware E2M1x2 conversion, INT4
+//     through mask-and-magic-number pairs -- and store them into tensor memory
+//     (tcgen05.st, one row per lane); the MMA reads its A operand from there, so
+//     shared memory only holds the packed codes and the activation rows and
+//     deep rings fit;
+//   * operands are fp16 x fp16: every dequantised weight is exact in fp16, and
+//     the activation operand keeps 11 significant bits.  Accumulation, bias,
+//     scales and the activation are fp32;
+//   * one producer thread keeps both streams in flight with TMA: a 1-D bulk
+//     copy of each stage's packed codes + scales (one contiguous chunk thanks to
+//     the repack) and a 2-D tile of the block's activation rows (GEMM1: the rows
+//     the prologue gathered in sorted order; GEMM2: GEMM1's output), landing in
+//     the 128-byte swizzled K-major layout;
+//   * a persistent grid (one CTA per SM) walks work items (tile, K-split, block)
+//     with the tile index fastest, so the tiles of one block run together and
+//     its activation rows are read from L2; K is split on the device when there
+//     are too few items to fill the GPU (decode), and the last CTA to arrive on
+//     an item's counter sums the fp32 partials in split order (bitwise
+//     reproducible, no spinning);
+//   * one thread issues tcgen05.mma into TMEM accumulators (double-buffered up
+//     to 64 tokens); eight epilogue warps (two per TMEM lane quarter, splitting
+//     the token columns) add bias and scales, apply the activation (GEMM1) or
+//     write rows to their pairs (GEMM2).
 #pragma once
+
+#include <cuda.h>
 
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kSA = 2;                 // dequantised-A ring
-constexpr int kSB = 4;                 // activation (B) ring
-constexpr int kSP = 8;                 // packed-weight ring
-constexpr int kBLoadAhead = 2;         // cp.async groups in flight in the loader
+constexpr int kSA = 4;                 // dequantised-A ring (in TMEM)
 constexpr int kNumDequantWarps = 8;
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpLoader = 2, kWarpDequant0 = 3;
-constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..14
-constexpr int kGemmThreads = (kWarpEpi0 + 4) * 32;          // 480
-constexpr int kHalfBytes = 128 * 128;                       // one 128-row x 64-K bf16 operand
+constexpr int kNumEpiWarps = 8;                             // two per TMEM lane quarter
+constexpr int kEpiThreads = kNumEpiWarps * 32;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpDequant0 = 2;
+constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 10..17
+constexpr int kGemmThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 576
 constexpr int kPackedSlotBytes = kPackedStageBytes + 1024;  // codes + largest scale block
+constexpr int kSmemBudget = 227 * 1024;
+constexpr uint32_t kTmemCols = 512;                         // whole TMEM (one CTA per SM)
+constexpr uint32_t kAColsPerStage = 64;                     // 2 halves x 64 K / 2 per column
 
 struct GemmArgs {
+  CUtensorMap tmap_b;         // activation rows [rows, Kred] 16-bit, 64 x BN boxes
   Layout L;
   const uint8_t* packed;      // repacked blob
-  const uint16_t* act;        // GEMM1: x bf16 [M, K]; GEMM2: a fp16 rows [cap, Npad]
-  int act_ld;                 // row stride of act in elements
   const int32_t* sorted_ids;
   const int32_t* expert_ids;
   const int32_t* n_padded;
   int pairs;                  // M * top_k (sentinel value)
-  int top_k;
   int block_m;
   int has_bias;
   int act_kind;               // moe_act
@@ -64,32 +71,39 @@ struct GemmArgs {
   int split_rows;             // rows of each split-K partial slice
   uint16_t* a_out;            // GEMM1 output, fp16 [cap, Npad]
   float* y_out;               // GEMM2 output, fp32 [pairs, K]
-  int32_t* inv_pos;           // GEMM2: pair -> sorted position
-  float* partial;             // split-K partials
-  int32_t* counters;          // GEMM1 split-K arrival counters [T1 * cap / block_m]
-  int32_t* split_used;        // GEMM2: chosen split (read by the combine)
+  float* partial;             // split-K partials [max_split][split_rows][width]
+  int32_t* counters;          // split-K arrival counters [T * blocks]
   unsigned* status;
 };
 
 template <int BN>
 struct GemmSmem {
-  static constexpr int kA = 0;
-  static constexpr int kB = kA + kSA * 2 * kHalfBytes;
+  static constexpr int kNacc = BN >= 128 ? 1 : 2;                                   // TMEM accumulators
+  static constexpr int kSB = BN <= 16 ? 16 : (BN <= 32 ? 12 : (BN <= 64 ? 8 : 6));  // activation ring
+  static constexpr int kB = 0;
   static constexpr int kP = kB + kSB * BN * 128;
+  static constexpr int kSPfit = (kSmemBudget - kP - 3072) / kPackedSlotBytes;
+  static constexpr int kSP = kSPfit > 16 ? 16 : kSPfit;  // packed-weight ring
   static constexpr int kBar = kP + kSP * kPackedSlotBytes;
-  // barriers: p_full, p_empty, a_full, a_empty, b_full, b_empty, acc_full[2], acc_empty[2], drain
-  static constexpr int kNumBars = 2 * kSP + 2 * kSA + 2 * kSB + 4 + 1;
-  static constexpr int kRows = kBar + kNumBars * 8;
-  static constexpr int kMisc = kRows + BN * 4;
+  // barriers: p_full, p_empty, a_full, a_empty, b_full, b_empty, acc_full, acc_empty, drain
+  static constexpr int kNumBars = 2 * kSP + 2 * kSA + 2 * kSB + 2 * kNacc + 1;
+  static constexpr int kEpiSid = kBar + kNumBars * 8;  // epilogue copy of the block's sorted ids
+  static constexpr int kMisc = kEpiSid + BN * 4;
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kSP >= 8, "packed ring too shallow");
+  static_assert(kAlloc <= 232448, "shared memory over the per-CTA limit");
+  static_assert(kSA * kAColsPerStage + kNacc * 2 * BN <= kTmemCols, "TMEM over budget");
 };
 
+// Gated activations in fp32 with the fast exponential and division intrinsics
+// (relative error ~1e-6, far inside the layer's tolerance); a very negative
+// gate gives 0 (its exponential overflows to +inf and the quotient to -0).
 __device__ __forceinline__ float act_fn(int kind, float g, float u, float alpha, float limit) {
-  if (kind == MOE_ACT_SILU_MUL) return g / (1.0f + __expf(-g)) * u;
+  if (kind == MOE_ACT_SILU_MUL) return __fdividef(g, 1.0f + __expf(-g)) * u;
   const float gc = fminf(g, limit);
   const float uc = fminf(fmaxf(u, -limit), limit);
-  return gc / (1.0f + __expf(-alpha * gc)) * (uc + 1.0f);
+  return __fdividef(gc, 1.0f + __expf(-alpha * gc)) * (uc + 1.0f);
 }
 
 struct WorkPlan {
@@ -107,27 +121,54 @@ __device__ __forceinline__ WorkPlan make_plan(const GemmArgs& g, bool gated) {
   const int stages = gated ? g.L.S1 : g.L.S2;
   p.units = stages / g.L.period;
   const int base = p.T * p.nb;
+  const int grid = (int)gridDim.x;
   int S = 1;
-  if (base > 0 && base < (int)gridDim.x) {
-    S = ((int)gridDim.x + base - 1) / base;
-    S = min(S, min(g.max_split, p.units));
-    if (p.nb * g.block_m > g.split_rows) S = 1;  // partial slices sized for this bound
+  if (base > 0 && base < grid && p.nb * g.block_m <= g.split_rows) {
+    // Cost in ninths of a weight stage (~9 KB streamed): every wave streams
+    // ceil(units/S) scale periods of weights; a split item also writes its fp32
+    // partial (2 x 128 rows x BN x 4 B ~ BN/9 stages) and the last CTA of each
+    // item reads S of them back.  Ties keep the smaller S.
+    const int bn = g.block_m < 16 ? 16 : g.block_m;
+    const int per = g.L.period;
+    int best = p.units * per * 9;  // S = 1: one wave of full-K items
+    const int smax = min(g.max_split, p.units);
+    for (int s = 2; s <= smax; ++s) {
+      const int waves = (base * s + grid - 1) / grid;
+      const int cost = waves * (((p.units + s - 1) / s) * per * 9 + bn) + s * bn;
+      if (cost < best) { best = cost; S = s; }
+    }
   }
   p.S = S;
   p.items = base * S;
   return p;
 }
 
+// item -> (block, tile, split), tile fastest
 __device__ __forceinline__ void decode_item(const WorkPlan& p, int w, int& b, int& tile, int& split) {
-  b = w % p.nb;
-  const int r = w / p.nb;
+  tile = w % p.T;
+  const int r = w / p.T;
   split = r % p.S;
-  tile = r / p.S;
+  b = r / p.S;
+}
+
+__device__ __forceinline__ void stage_range(const WorkPlan& p, const Layout& L, int split, int& s0, int& s1) {
+  s0 = split * p.units / p.S * L.period;
+  s1 = (split + 1) * p.units / p.S * L.period;
+}
+
+// TMA: a 2-D tile (box from the tensor map) at (col, row).
+__device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap* map, int col, int row, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(row), "r"(smem_u32(bar))
+      : "memory");
 }
 
 template <int FMT, bool GATED, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
   using SM = GemmSmem<BN>;
+  constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBar);
@@ -138,23 +179,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   uint64_t* b_full = a_empty + kSA;
   uint64_t* b_empty = b_full + kSB;
   uint64_t* acc_full = b_empty + kSB;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain_bar = acc_empty + 2;
-  int32_t* row_tab = reinterpret_cast<int32_t*>(smem + SM::kRows);
+  uint64_t* acc_empty = acc_full + kNacc;
+  uint64_t* drain_bar = acc_empty + kNacc;
+  int32_t* epi_sid = reinterpret_cast<int32_t*>(smem + SM::kEpiSid);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + SM::kMisc);  // [0] tmem base, [1] abort, [2] last flag
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[1]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Layout& L = g.L;
-  constexpr uint32_t kTmemCols = (4 * BN) < 32 ? 32 : 4 * BN;  // two accumulators of 2*BN columns
-  constexpr bool kF16 = (FMT == MOE_W_INT4_U4B8) || !GATED;   // fp16 operands, else bf16
-  constexpr bool kConvertB = GATED && FMT == MOE_W_INT4_U4B8;  // bf16 input rows -> fp16 in smem
+  constexpr uint32_t kBBytes = BN * 128;                      // activation bytes per stage
+  constexpr uint32_t kAccCol0 = kSA * kAColsPerStage;        // accumulators after the A ring
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], kNumDequantWarps); }
     for (int i = 0; i < kSA; ++i) { mbar_init(&a_full[i], kNumDequantWarps); mbar_init(&a_empty[i], 1); }
     for (int i = 0; i < kSB; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+    for (int i = 0; i < kNacc; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kNumEpiWarps); }
     mbar_init(drain_bar, 1);
     misc[1] = 0;
     fence_mbar_init();
@@ -163,117 +203,80 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     tmem_alloc(&misc[0], kTmemCols);
     tmem_relinquish();
   }
+  if (warp == kWarpProducer && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g.tmap_b)) : "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
 
   const WorkPlan plan = make_plan(g, GATED);
-  if (GATED == false && blockIdx.x == 0 && threadIdx.x == 0) *g.split_used = plan.S;
   const int64_t tile_bytes = GATED ? L.tile1_bytes : L.tile2_bytes;
   const uint8_t* wbase = g.packed + (GATED ? L.w13_off : L.w2_off);
 
   if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (weights + activation rows)
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      uint32_t pk = 0;
+      uint32_t pk = 0, bk = 0;
       for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
-        int b, tile, split;
+        int b, tile, split, s0, s1;
         decode_item(plan, w, b, tile, split);
+        stage_range(plan, L, split, s0, s1);
         const int e = g.expert_ids[b];
-        const int s0 = split * plan.units / plan.S * L.period, s1 = (split + 1) * plan.units / plan.S * L.period;
         const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
-        for (int s = s0; s < s1; ++s, ++pk) {
+        for (int s = s0; s < s1; ++s, ++pk, ++bk) {
           const int slot = pk % kSP;
           mbar_wait(&p_empty[slot], ((pk / kSP) + 1) & 1, abort_flag, g.status);
           const int bytes = stage_bytes(L, s);
           mbar_arrive_expect_tx(&p_full[slot], bytes);
           bulk_g2s(smem + SM::kP + slot * kPackedSlotBytes, tb + stage_offset(L, s), bytes, &p_full[slot], pol);
+          const int bs = bk % kSB;
+          mbar_wait(&b_empty[bs], ((bk / kSB) + 1) & 1, abort_flag, g.status);
+          mbar_arrive_expect_tx(&b_full[bs], kBBytes);
+          tma_tile2d(smem_u32(smem + SM::kB + bs * kBBytes), &g.tmap_b, s * kStageK, b * g.block_m, &b_full[bs]);
         }
       }
       // leave no copy in flight: wait for the last phase of every used slot
-      for (uint32_t i = 0; i < kSP && i < pk; ++i) {
+      for (uint32_t i = 0; i < (uint32_t)kSP && i < pk; ++i) {
         const uint32_t k = pk - 1 - i;
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(&p_full[k % kSP], (k / kSP) & 1) && global_timer_ns() - t0 < 100000000ull) {
         }
       }
-    }
-  } else if (warp == kWarpLoader) {
-    // ------------------------------------------------------------ activation rows (cp.async)
-    uint32_t bk = 0, retired = 0;
-    for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
-      int b, tile, split;
-      decode_item(plan, w, b, tile, split);
-      const int s0 = split * plan.units / plan.S * L.period, s1 = (split + 1) * plan.units / plan.S * L.period;
-      __syncwarp();
-      for (int j = lane; j < BN; j += 32) {
-        int row = -1;
-        if (j < g.block_m) {
-          if (GATED) {
-            const int sid = g.sorted_ids[b * g.block_m + j];
-            row = sid < g.pairs ? sid / g.top_k : -1;
-          } else {
-            row = b * g.block_m + j;
-          }
-        }
-        row_tab[j] = row;
-      }
-      __syncwarp();
-      for (int s = s0; s < s1; ++s, ++bk) {
-        const int slot = bk % kSB;
-        mbar_wait(&b_empty[slot], ((bk / kSB) + 1) & 1, abort_flag, g.status);
-        const uint32_t dst0 = smem_u32(smem + SM::kB + slot * BN * 128);
-        for (int c = lane; c < BN * 8; c += 32) {
-          const int j = c >> 3, ck = c & 7;
-          const int row = row_tab[j];
-          const uint16_t* src = g.act + (row >= 0 ? (int64_t)row * g.act_ld + s * kStageK + ck * 8 : 0);
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst0 + sw128_offset(j, ck)), "l"(src),
-                       "r"(row >= 0 ? 16 : 0)
-                       : "memory");
-        }
-        cp_async_commit();
-        if (bk + 1 - retired > kBLoadAhead) {
-          cp_async_wait<kBLoadAhead>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&b_full[retired % kSB]);
-          ++retired;
+      for (uint32_t i = 0; i < (uint32_t)kSB && i < bk; ++i) {
+        const uint32_t k = bk - 1 - i;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&b_full[k % kSB], (k / kSB) & 1) && global_timer_ns() - t0 < 100000000ull) {
         }
       }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    for (; retired < bk; ++retired)
-      if (lane == 0) mbar_arrive(&b_full[retired % kSB]);
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(128, BN, kF16 ? 0u : 1u);
+      constexpr uint32_t idesc = idesc_f16_f32(128, BN, 0u);
       uint32_t ak = 0, bk = 0, ic = 0;
-      const uint32_t a0 = smem_u32(smem + SM::kA), b0 = smem_u32(smem + SM::kB);
+      const uint32_t b0 = smem_u32(smem + SM::kB);
       for (int w = blockIdx.x; w < plan.items; w += gridDim.x, ++ic) {
-        int b, tile, split;
+        int b, tile, split, s0, s1;
         decode_item(plan, w, b, tile, split);
-        const int s0 = split * plan.units / plan.S * L.period, s1 = (split + 1) * plan.units / plan.S * L.period;
-        const int accb = ic & 1;
-        mbar_wait(&acc_empty[accb], ((ic >> 1) + 1) & 1, abort_flag, g.status);
+        stage_range(plan, L, split, s0, s1);
+        const int accb = ic % kNacc;
+        mbar_wait(&acc_empty[accb], ((ic / kNacc) + 1) & 1, abort_flag, g.status);
         tc_fence_after();
-        const uint32_t d0 = tmem_base + accb * 2 * BN;
+        const uint32_t d0 = tmem_base + kAccCol0 + accb * 2 * BN;
         for (int s = s0; s < s1; ++s, ++ak, ++bk) {
           const int as = ak % kSA, bs = bk % kSB;
           mbar_wait(&a_full[as], (ak / kSA) & 1, abort_flag, g.status);
-          if (!kConvertB) mbar_wait(&b_full[bs], (bk / kSB) & 1, abort_flag, g.status);
+          mbar_wait(&b_full[bs], (bk / kSB) & 1, abort_flag, g.status);
           tc_fence_after();
-          const uint32_t abase = a0 + as * 2 * kHalfBytes, bbase = b0 + bs * BN * 128;
+          const uint32_t a_t = tmem_base + as * kAColsPerStage, bbase = b0 + bs * kBBytes;
 #pragma unroll
           for (int kk = 0; kk < kStageK / 16; ++kk) {
             const uint64_t bd = smem_desc_sw128(bbase + kk * 32);
             const uint32_t acc = (s > s0 || kk > 0) ? 1u : 0u;
-            umma_bf16(d0, smem_desc_sw128(abase + kk * 32), bd, idesc, acc);
-            umma_bf16(d0 + BN, smem_desc_sw128(abase + kHalfBytes + kk * 32), bd, idesc, acc);
+            umma_f16_tmem_a(d0, a_t + kk * 8, bd, idesc, acc);
+            umma_f16_tmem_a(d0 + BN, a_t + 32 + kk * 8, bd, idesc, acc);
           }
           umma_commit(&a_empty[as]);
           umma_commit(&b_empty[bs]);
@@ -288,14 +291,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant warps
-    const int r = threadIdx.x - kWarpDequant0 * 32;  // tile row 0..255
-    const int half = r >> 7, hr = r & 127;
+    // warp -> (TMEM lane quarter q = warp % 4, half): a warp may only touch TMEM
+    // lanes 32q..32q+31; each thread dequantises one tile row per stage
+    const int q = warp & 3, half = (warp - kWarpDequant0) >> 2;
+    const int hr = q * 32 + lane;   // row within the half = TMEM lane
+    const int r = half * 128 + hr;  // tile row
+    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + half * 32;
     uint32_t pk = 0, ak = 0;
-    uint32_t mult[4] = {0, 0, 0, 0};  // per-stage multipliers (bf16x2)
+    uint32_t m[4] = {0, 0, 0, 0};  // f16x2 multipliers (INT4: s, s/16; MXFP4: per 32; NVFP4: per 16)
     for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
-      int b, tile, split;
+      int b, tile, split, s0, s1;
       decode_item(plan, w, b, tile, split);
-      const int s0 = split * plan.units / plan.S * L.period, s1 = (split + 1) * plan.units / plan.S * L.period;
+      stage_range(plan, L, split, s0, s1);
       for (int s = s0; s < s1; ++s, ++pk, ++ak) {
         const int ps = pk % kSP, as = ak % kSA;
         mbar_wait(&p_full[ps], (pk / kSP) & 1, abort_flag, g.status);
@@ -303,65 +310,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         const bool has_sc = stage_has_scales(L, s);
         if (has_sc) {
           if (FMT == MOE_W_INT4_U4B8) {
-            const uint32_t sv = reinterpret_cast<const uint16_t*>(slot)[r];
-            const uint32_t m = kF16 ? bf16_scale_f16(sv) : sv;
-            mult[0] = m | (m << 16);
+            const uint32_t h = bf16_scale_f16(reinterpret_cast<const uint16_t*>(slot)[r]);
+            const uint32_t h16 = __half_as_ushort(__hmul(__ushort_as_half((uint16_t)h), __ushort_as_half(0x2C00)));
+            m[0] = h | (h << 16);      // s
+            m[1] = h16 | (h16 << 16);  // s / 16
           } else if (FMT == MOE_W_MXFP4) {
             const uint32_t sv = reinterpret_cast<const uint16_t*>(slot)[r];
-            const uint32_t m0 = kF16 ? e8m0_mult_f16(sv & 0xFF) : e8m0_mult_bits(sv & 0xFF);
-            const uint32_t m1 = kF16 ? e8m0_mult_f16(sv >> 8) : e8m0_mult_bits(sv >> 8);
-            mult[0] = m0 | (m0 << 16);
-            mult[1] = m1 | (m1 << 16);
+            const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
+            m[0] = a | (a << 16);
+            m[1] = c | (c << 16);
           } else {
             const uint32_t sv = reinterpret_cast<const uint32_t*>(slot)[r];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t b8 = (sv >> (8 * q)) & 0xFF;
-              const uint32_t m = kF16 ? e4m3_mult_f16(b8) : e4m3_mult_bits(b8);
-              mult[q] = m | (m << 16);
-            }
+            const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
+            m[0] = __byte_perm(lo, 0, 0x1010);
+            m[1] = __byte_perm(lo, 0, 0x3232);
+            m[2] = __byte_perm(hi, 0, 0x1010);
+            m[3] = __byte_perm(hi, 0, 0x3232);
           }
         }
-        const uint4* codes = reinterpret_cast<const uint4*>(slot + (has_sc ? L.scale_bytes : 0));
-        const uint4 u0 = codes[r], u1 = codes[256 + r];
+        const uint4* units = reinterpret_cast<const uint4*>(slot + (has_sc ? L.scale_bytes : 0));
+        const uint4 u0 = units[r], u1 = units[256 + r];
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[ps]);
+        const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        uint32_t o[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t t4[4];
+          if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[i], m[0], m[1], t4);
+          else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[i], m[i >> 2], m[i >> 2], t4);
+          else e2m1x8_f16(wd[i], m[i >> 1], m[i >> 1], t4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[4 * i + k] = t4[k];
+        }
         mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
-        const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        const uint32_t dst = smem_u32(smem + SM::kA + as * 2 * kHalfBytes + half * kHalfBytes);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t m2;
-          if (FMT == MOE_W_INT4_U4B8) m2 = mult[0];
-          else if (FMT == MOE_W_MXFP4) m2 = mult[c >> 2];
-          else m2 = mult[c >> 1];
-          uint32_t o[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (FMT == MOE_W_INT4_U4B8)
-              o[i] = kF16 ? dq_int4_pair_f16(words[c], i, m2) : dq_int4_pair(words[c], i, m2);
-            else
-              o[i] = kF16 ? dq_e2m1_pair_f16(words[c], i, m2) : dq_e2m1_pair(words[c], i, m2);
-          }
-          st_shared_v4(dst + sw128_offset(hr, c), o[0], o[1], o[2], o[3]);
-        }
-        if (kConvertB) {
-          // the staged bf16 input rows of this stage -> fp16, in place
-          const int bs = ak % kSB;
-          mbar_wait(&b_full[bs], (ak / kSB) & 1, abort_flag, g.status);
-          const uint32_t bbase = smem_u32(smem + SM::kB + bs * BN * 128);
-          for (int c = r; c < BN * 8; c += 256) {
-            const uint32_t addr = bbase + c * 16;
-            uint32_t v0, v1, v2, v3;
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
-                         : "r"(addr)
-                         : "memory");
-            st_shared_v4(addr, bf16x2_to_f16x2(v0), bf16x2_to_f16x2(v1), bf16x2_to_f16x2(v2),
-                         bf16x2_to_f16x2(v3));
-          }
-        }
-        fence_proxy_async_smem();
+        tc_fence_after();
+        tmem_st32(t_lane + as * kAColsPerStage, o);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[as]);
       }
@@ -370,24 +356,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;            // TMEM lane quarter
     const int hr = q * 32 + lane;      // row within each 128-row half
-    const int et = threadIdx.x - kWarpEpi0 * 32;  // 0..127
+    const int et = threadIdx.x - kWarpEpi0 * 32;  // 0..255
+    const int csub = (warp - kWarpEpi0) >> 2;      // which 8-column chunks this warp takes
     const float* gs_tab = reinterpret_cast<const float*>(g.packed + (GATED ? L.gs13_off : L.gs2_off));
     const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (GATED ? L.b13_off : L.b2_off));
     const int Npad = L.Npad;
+    const int width = GATED ? 2 * Npad : L.K;  // partial row width
     uint32_t ic = 0;
     for (int w = blockIdx.x; w < plan.items; w += gridDim.x, ++ic) {
       int b, tile, split;
       decode_item(plan, w, b, tile, split);
+      // everything the item's epilogue reads from global memory is fetched before
+      // the accumulator wait, off the critical path
+      const int jmax = min(BN, g.block_m);
+      named_bar_sync(2, kEpiThreads);  // the previous item's readers of epi_sid are done
+      if (et < jmax) epi_sid[et] = g.sorted_ids[b * g.block_m + et];
       const int e = g.expert_ids[b];
       const float gsc = gs_tab[e];
-      const int accb = ic & 1;
-      mbar_wait(&acc_full[accb], (ic >> 1) & 1, abort_flag, g.status);
-      tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + accb * 2 * BN;
-      // feature / output rows held by this thread in half 0 and half 1
-      int row0, row1;
-      if (GATED) { row0 = tile * 128 + hr; row1 = row0; }
-      else { row0 = tile * 256 + hr; row1 = row0 + 128; }
+      // feature / output rows held by this thread in half 0 and half 1; for
+      // GEMM1 both halves hold the same feature (gate and up)
+      int row0, row1, col0, col1;  // col*: index in the partial row
+      if (GATED) { row0 = tile * 128 + hr; row1 = row0; col0 = row0; col1 = Npad + row0; }
+      else { row0 = tile * 256 + hr; row1 = row0 + 128; col0 = row0; col1 = row1; }
       float bias0 = 0.f, bias1 = 0.f;
       if (g.has_bias) {
         if (GATED) {
@@ -398,81 +388,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           bias1 = bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + row1]);
         }
       }
-      const int jmax = min(BN, g.block_m);
+      const bool ok0 = GATED || row0 < L.K, ok1 = GATED || row1 < L.K;
+      named_bar_sync(2, kEpiThreads);
+      const int accb = ic % kNacc;
+      mbar_wait(&acc_full[accb], (ic / kNacc) & 1, abort_flag, g.status);
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + kAccCol0 + accb * 2 * BN;
       bool finish = true;  // this CTA writes final results for the item
       if (plan.S > 1) {
         // split-K: store the fp32 partial of this slice, rows by sorted position
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tb + c0, v0);
-          tmem_ld16(tb + BN + c0, v1);
+        for (int c0 = 8 * csub; c0 < BN; c0 += 16) {
+          uint32_t v0[8], v1[8];
+          tmem_ld8(tb + c0, v0);
+          tmem_ld8(tb + BN + c0, v1);
           tmem_ld_wait();
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
+          for (int jj = 0; jj < 8; ++jj) {
             if (c0 + jj >= jmax) break;
-            const int pos = b * g.block_m + c0 + jj;
-            if (GATED) {
-              float* dst = g.partial + ((int64_t)split * g.split_rows + pos) * 2 * Npad;
-              __stcg(dst + row0, __uint_as_float(v0[jj]));
-              __stcg(dst + Npad + row1, __uint_as_float(v1[jj]));
-            } else {
-              float* dst = g.partial + ((int64_t)split * g.split_rows + pos) * L.K;
-              if (row0 < L.K) __stcg(dst + row0, __uint_as_float(v0[jj]));
-              if (row1 < L.K) __stcg(dst + row1, __uint_as_float(v1[jj]));
-            }
+            float* dst = g.partial + ((int64_t)split * g.split_rows + b * g.block_m + c0 + jj) * width;
+            if (ok0) __stcg(dst + col0, __uint_as_float(v0[jj]));
+            if (ok1) __stcg(dst + col1, __uint_as_float(v1[jj]));
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[accb]);
-        if (GATED) {
-          __threadfence();
-          named_bar_sync(1, 128);
-          if (et == 0) {
-            const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[tile * (*g.n_padded / g.block_m) + b]),
-                                           (unsigned)(plan.S - 1));
-            misc[2] = old == (unsigned)(plan.S - 1) ? 1u : 0u;
-          }
-          named_bar_sync(1, 128);
-          finish = misc[2] != 0;
-          if (finish) __threadfence();
-        } else {
-          finish = false;  // the combine reduces GEMM2 partials
+        __threadfence();
+        named_bar_sync(1, kEpiThreads);
+        if (et == 0) {
+          const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[b * plan.T + tile]),
+                                         (unsigned)(plan.S - 1));
+          misc[2] = old == (unsigned)(plan.S - 1) ? 1u : 0u;
         }
-      }
-      if (!GATED && tile == 0 && split == 0) {
-        for (int j = et; j < g.block_m; j += 128) {
-          const int sid = g.sorted_ids[b * g.block_m + j];
-          if (sid < g.pairs) g.inv_pos[sid] = b * g.block_m + j;
-        }
+        named_bar_sync(1, kEpiThreads);
+        finish = misc[2] != 0;
+        if (finish) __threadfence();
       }
       if (finish) {
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          float f0[16], f1[16];
+        for (int c0 = 8 * csub; c0 < BN; c0 += 16) {
+          float f0[8], f1[8];
           if (plan.S == 1) {
-            uint32_t v0[16], v1[16];
-            tmem_ld16(tb + c0, v0);
-            tmem_ld16(tb + BN + c0, v1);
+            uint32_t v0[8], v1[8];
+            tmem_ld8(tb + c0, v0);
+            tmem_ld8(tb + BN + c0, v1);
             tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) { f0[jj] = __uint_as_float(v0[jj]); f1[jj] = __uint_as_float(v1[jj]); }
+            for (int jj = 0; jj < 8; ++jj) { f0[jj] = __uint_as_float(v0[jj]); f1[jj] = __uint_as_float(v1[jj]); }
           } else {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) { f0[jj] = 0.f; f1[jj] = 0.f; }
+            for (int jj = 0; jj < 8; ++jj) { f0[jj] = 0.f; f1[jj] = 0.f; }
             for (int sp = 0; sp < plan.S; ++sp)
 #pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
+              for (int jj = 0; jj < 8; ++jj) {
                 if (c0 + jj >= jmax) break;
-                const float* src = g.partial + ((int64_t)sp * g.split_rows + b * g.block_m + c0 + jj) * 2 * Npad;
-                f0[jj] += __ldcg(src + row0);
-                f1[jj] += __ldcg(src + Npad + row1);
+                const float* src = g.partial + ((int64_t)sp * g.split_rows + b * g.block_m + c0 + jj) * width;
+                if (ok0) f0[jj] += __ldcg(src + col0);
+                if (ok1) f1[jj] += __ldcg(src + col1);
               }
           }
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
+          for (int jj = 0; jj < 8; ++jj) {
             if (c0 + jj >= jmax) break;
             const int pos = b * g.block_m + c0 + jj;
-            const int sid = g.sorted_ids[pos];
+            const int sid = epi_sid[c0 + jj];
             if (GATED) {
               const float hg = f0[jj] * gsc + bias0;
               const float hu = f1[jj] * gsc + bias1;
@@ -480,8 +458,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               g.a_out[(int64_t)pos * Npad + row0] = __half_as_ushort(__float2half_rn(a));
             } else if (sid < g.pairs) {
               float* dst = g.y_out + (int64_t)sid * L.K;
-              if (row0 < L.K) dst[row0] = f0[jj] * gsc + bias0;
-              if (row1 < L.K) dst[row1] = f1[jj] * gsc + bias1;
+              if (ok0) dst[row0] = f0[jj] * gsc + bias0;
+              if (ok1) dst[row1] = f1[jj] * gsc + bias1;
             }
           }
         }

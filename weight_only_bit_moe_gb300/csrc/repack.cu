@@ -72,7 +72,10 @@ __global__ void repack_codes_kernel(RepackArgs a, int which) {
           const uint8_t b = srow[k >> 1];
           q = (k & 1) ? (b >> 4) : (b & 15u);
         }
-        const int pos = (el & 1) ? 16 + 4 * (el >> 1) : 4 * (el >> 1);
+        // INT4: element 2i at bits 4i, 2i+1 at bits 16 + 4i (mask-and-magic pairs);
+        // FP4: element order, byte i = elements 2i (low nibble), 2i+1 (high), as the
+        // hardware E2M1x2 conversion reads them
+        const int pos = L.fmt == MOE_W_INT4_U4B8 ? ((el & 1) ? 16 + 4 * (el >> 1) : 4 * (el >> 1)) : 4 * el;
         word |= q << pos;
       }
       words[w] = word;
