@@ -400,7 +400,11 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.sweep:
         import torch
-        for name, M in SWEEP:
+        sweep = SWEEP
+        if os.environ.get("MOE_SWEEP_ONLY"):
+            keep = set(os.environ["MOE_SWEEP_ONLY"].split(","))
+            sweep = [(n, m) for n, m in SWEEP if f"{n}:{m}" in keep]
+        for name, M in sweep:
             args.workload, args.M = name, M
             line = run_ours(args, 0, 1)
             print(json.dumps(line), flush=True)
