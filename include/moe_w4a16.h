@@ -163,6 +163,43 @@ int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void
                       float routed_scaling_factor, const void* post_norm_w, float norm_eps,
                       void* out, void* workspace, int64_t workspace_bytes, void* stream);
 
+/* Allocation-free forward.  Not part of the method: the pages have no
+ * counterpart; it exists for callers that cannot pass device memory of their
+ * own, such as code running on a stream that a framework is recording into a
+ * CUDA graph (an allocation there breaks the recording) or plugins of an engine
+ * that owns every device allocation.
+ *   Same computation, arguments and rules as moe_w4a16_forward, without
+ * workspace / workspace_bytes.  The workspace is instead a fixed array of
+ * MOE_NOALLOC_SCRATCH_BYTES in this library's device image, one per device and
+ * process, reserved by the CUDA runtime when the module loads; no call here
+ * allocates device memory.  Its split-K partial areas are smaller than those
+ * moe_w4a16_forward plans, so this entry point can pick fewer K splits;
+ * results match moe_w4a16_forward's within the layer's tolerance, not bit for
+ * bit.
+ *   Size limit: returns MOE_ERR_WORKSPACE (nothing launched) when the shape's
+ * workspace would exceed MOE_NOALLOC_SCRATCH_BYTES; moe_w4a16_forward with a
+ * caller workspace handles such shapes.
+ *   Start state: none needed.  The prologue kernel zeroes the status word and
+ * the split-K counters at the start of every call.
+ *   Concurrency: calls on one device share the array, so two calls in flight
+ * at once (two streams, or two host threads without ordering) race and give
+ * undefined results; the caller serialises them.
+ *   Setup: the first call on a device looks up the array's address
+ * (cudaGetSymbolAddress, which can load the module) and the tensor-map
+ * encoder; make one call on each device before any stream capture.  Nothing
+ * is claimed about behaviour under capture.
+ *   Status: a device wait that runs out of iterations is recorded in the
+ * array's status word, which this entry point does not report; callers that
+ * need that report use moe_w4a16_forward and moe_get_status. */
+#define MOE_NOALLOC_SCRATCH_BYTES ((int64_t)64 << 20)
+int moe_w4a16_forward_noalloc(const moe_layer_desc* desc, const void* packed, const void* x,
+                              int M, int top_k, const int32_t* topk_ids,
+                              const float* topk_weights, int expert_base,
+                              const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* n_padded, int block_m, int act, float alpha,
+                              float limit, float routed_scaling_factor, const void* post_norm_w,
+                              float norm_eps, void* out, void* stream);
+
 /* Synchronises `stream`, returns the device status recorded in `workspace` by
  * earlier forwards on it (MOE_OK or MOE_ERR_TIMEOUT) and clears it. */
 int moe_get_status(void* workspace, void* stream);

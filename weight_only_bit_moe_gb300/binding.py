@@ -20,8 +20,9 @@ MOE_W_INT4_U4B8, MOE_W_MXFP4, MOE_W_NVFP4 = 0, 1, 2
 MOE_ACT_SILU_MUL, MOE_ACT_SIGMOID_ALPHA = 0, 1
 
 EXPORTED = ("moe_repack_size", "moe_repack_weights", "moe_align_capacity", "moe_align", "moe_choose_block_m",
-            "moe_workspace_size", "moe_w4a16_forward", "moe_get_status", "moe_set_trace_events",
-            "moe_status_string")
+            "moe_workspace_size", "moe_w4a16_forward", "moe_w4a16_forward_noalloc", "moe_get_status",
+            "moe_set_trace_events", "moe_status_string")
+MOE_NOALLOC_SCRATCH_BYTES = 64 << 20  # fixed workspace of moe_w4a16_forward_noalloc
 
 
 class MoeError(RuntimeError):
@@ -62,6 +63,8 @@ def load(path: str = ""):
                 "moe_workspace_size": (i64, [D, i32, i32, i32]),
                 "moe_w4a16_forward": (i32, [D, p, p, i32, i32, p, p, i32, p, p, p, i32, i32, f32, f32, f32, p,
                                             f32, p, p, i64, p]),
+                "moe_w4a16_forward_noalloc": (i32, [D, p, p, i32, i32, p, p, i32, p, p, p, i32, i32, f32, f32, f32,
+                                                    p, f32, p, p]),
                 "moe_get_status": (i32, [p, p]),
                 "moe_set_trace_events": (i32, [ctypes.POINTER(ctypes.c_void_p), i32]),
                 "moe_status_string": (ctypes.c_char_p, [i32]),
@@ -149,6 +152,20 @@ def moe_w4a16_forward(desc, packed, x, M, top_k, topk_ids, topk_weights, expert_
         ctypes.byref(desc), _p(packed), _p(x), M, top_k, _p(topk_ids), _p(topk_weights), expert_base,
         _p(sorted_ids), _p(expert_ids), _p(n_padded), block_m, act, alpha, limit, routed_scaling_factor,
         _p(post_norm_w), norm_eps, _p(out), _p(workspace), workspace_bytes, _stream(stream)))
+
+
+def moe_w4a16_forward_noalloc(desc, packed, x, M, top_k, topk_ids, topk_weights, expert_base, sorted_ids,
+                              expert_ids, n_padded, block_m, act, alpha, limit, routed_scaling_factor, post_norm_w,
+                              norm_eps, out, stream=None):
+    """moe_w4a16_forward on the library's fixed device scratch (no workspace argument)."""
+    rc = load().moe_w4a16_forward_noalloc(
+        ctypes.byref(desc), _p(packed), _p(x), M, top_k, _p(topk_ids), _p(topk_weights), expert_base,
+        _p(sorted_ids), _p(expert_ids), _p(n_padded), block_m, act, alpha, limit, routed_scaling_factor,
+        _p(post_norm_w), norm_eps, _p(out), _stream(stream))
+    if rc == MOE_ERR_WORKSPACE:
+        raise MoeError("moe_w4a16_forward_noalloc (shape needs more than the "
+                       f"{MOE_NOALLOC_SCRATCH_BYTES >> 20} MiB fixed scratch)", rc)
+    return _check("moe_w4a16_forward_noalloc", rc)
 
 
 def moe_get_status(workspace, stream=None) -> int:

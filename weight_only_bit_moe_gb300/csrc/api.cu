@@ -7,6 +7,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "combine.cuh"
 #include "gemm_launch.cuh"
 #include "prep.cuh"
@@ -37,7 +39,8 @@ struct WsPlan {
       total;
 };
 
-bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w) {
+bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
+                    int64_t split_budget = kSplitBudgetBytes) {
   const int64_t cap = moe_align_capacity(M, top_k, L.E, block_m);
   if (cap < 0) return false;
   const int grid = device_sm_count();
@@ -50,8 +53,8 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w) {
   w->rows1 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T1 + 1) * block_m);
   w->rows2 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T2 + 1) * block_m);
   const int64_t per1 = (int64_t)w->rows1 * 2 * L.Npad * 4, per2 = (int64_t)w->rows2 * L.K * 4;
-  w->max_split1 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per1 ? kSplitBudgetBytes / per1 : 1));
-  w->max_split2 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per2 ? kSplitBudgetBytes / per2 : 1));
+  w->max_split1 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per1 ? split_budget / per1 : 1));
+  w->max_split2 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per2 ? split_budget / per2 : 1));
   int64_t off = 0;
   w->status_off = off;
   off += 256;
@@ -143,28 +146,33 @@ extern "C" int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top
   return w.total;
 }
 
-extern "C" int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void* x, int M, int top_k,
-                                 const int32_t* topk_ids, const float* topk_weights, int expert_base,
-                                 const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* n_padded,
-                                 int block_m, int act, float alpha, float limit, float routed_scaling_factor,
-                                 const void* post_norm_w, float norm_eps, void* out, void* workspace,
-                                 int64_t workspace_bytes, void* stream) {
-  Layout L;
-  if (!desc || !make_layout(*desc, &L)) return MOE_ERR_INVALID;
+namespace moe {
+
+// Argument rules shared by both forward entry points (everything but the workspace).
+static int check_forward_args(const moe_layer_desc* desc, const void* packed, const void* x, int M, int top_k,
+                              const int32_t* topk_ids, const float* topk_weights, const int32_t* sorted_ids,
+                              const int32_t* expert_ids, const int32_t* n_padded, int block_m, int act,
+                              const void* post_norm_w, const void* out, Layout* L) {
+  if (!desc || !make_layout(*desc, L)) return MOE_ERR_INVALID;
   if (M < 0 || top_k <= 0 || top_k > 16 || !valid_block_m(block_m)) return MOE_ERR_INVALID;
   if (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SIGMOID_ALPHA) return MOE_ERR_INVALID;
   if ((int64_t)M * top_k >= (int64_t)1 << 31) return MOE_ERR_INVALID;
   if (M == 0) return MOE_OK;
-  if (!packed || !x || !topk_ids || !topk_weights || !sorted_ids || !expert_ids || !n_padded || !out ||
-      !workspace)
+  if (!packed || !x || !topk_ids || !topk_weights || !sorted_ids || !expert_ids || !n_padded || !out)
     return MOE_ERR_INVALID;
-  if ((reinterpret_cast<uintptr_t>(packed) & 255) || (reinterpret_cast<uintptr_t>(workspace) & 255) ||
-      (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
-      (reinterpret_cast<uintptr_t>(post_norm_w) & 15))
+  if ((reinterpret_cast<uintptr_t>(packed) & 255) || (reinterpret_cast<uintptr_t>(x) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 15) || (reinterpret_cast<uintptr_t>(post_norm_w) & 15))
     return MOE_ERR_INVALID;
-  WsPlan w;
-  if (!plan_workspace(L, M, top_k, block_m, &w)) return MOE_ERR_CUDA;
-  if (workspace_bytes < w.total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// The launch sequence on a checked argument set and a workspace laid out by `w`.
+static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPlan& w, const void* packed,
+                        const void* x, int M, int top_k, const int32_t* topk_ids, const float* topk_weights,
+                        int expert_base, const int32_t* sorted_ids, const int32_t* expert_ids,
+                        const int32_t* n_padded, int block_m, int act, float alpha, float limit,
+                        float routed_scaling_factor, const void* post_norm_w, float norm_eps, void* out,
+                        void* workspace, void* stream) {
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
@@ -242,6 +250,80 @@ extern "C" int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed,
   if (launch_combine(c, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(3, st) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void* x, int M, int top_k,
+                                 const int32_t* topk_ids, const float* topk_weights, int expert_base,
+                                 const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* n_padded,
+                                 int block_m, int act, float alpha, float limit, float routed_scaling_factor,
+                                 const void* post_norm_w, float norm_eps, void* out, void* workspace,
+                                 int64_t workspace_bytes, void* stream) {
+  Layout L;
+  const int rc = check_forward_args(desc, packed, x, M, top_k, topk_ids, topk_weights, sorted_ids, expert_ids,
+                                    n_padded, block_m, act, post_norm_w, out, &L);
+  if (rc != MOE_OK || M == 0) return rc;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return MOE_ERR_INVALID;
+  WsPlan w;
+  if (!plan_workspace(L, M, top_k, block_m, &w)) return MOE_ERR_CUDA;
+  if (workspace_bytes < w.total) return MOE_ERR_WORKSPACE;
+  return forward_impl(desc, L, w, packed, x, M, top_k, topk_ids, topk_weights, expert_base, sorted_ids, expert_ids,
+                      n_padded, block_m, act, alpha, limit, routed_scaling_factor, post_norm_w, norm_eps, out,
+                      workspace, stream);
+}
+
+// Allocation-free variant.  Some callers cannot hand over device memory of
+// their own: code that runs inside a stream that a framework is recording into
+// a graph, where a cudaMalloc would break the recording, or plugins of an
+// engine that owns every device allocation.  For them the workspace is a fixed
+// array in this library's device image, reserved by the CUDA runtime when the
+// module loads, so no call here allocates.  One array per device and process:
+// two calls in flight at once (two streams, two host threads) share it and
+// race.  The prologue kernel zeroes the status word and the split-K counters
+// on every call, so the array needs no initialisation.
+namespace moe {
+
+constexpr int64_t kNoAllocScratchBytes = MOE_NOALLOC_SCRATCH_BYTES;
+// smaller split-K partial areas than the caller-workspace path so that the
+// usual shapes fit in the fixed array
+constexpr int64_t kNoAllocSplitBudget = 4ll << 20;
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array on the current device, looked up once per device.
+void* noalloc_scratch() {
+  static std::atomic<void*> cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    cache[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+}  // namespace moe
+
+extern "C" int moe_w4a16_forward_noalloc(const moe_layer_desc* desc, const void* packed, const void* x, int M,
+                                         int top_k, const int32_t* topk_ids, const float* topk_weights,
+                                         int expert_base, const int32_t* sorted_ids, const int32_t* expert_ids,
+                                         const int32_t* n_padded, int block_m, int act, float alpha, float limit,
+                                         float routed_scaling_factor, const void* post_norm_w, float norm_eps,
+                                         void* out, void* stream) {
+  Layout L;
+  const int rc = check_forward_args(desc, packed, x, M, top_k, topk_ids, topk_weights, sorted_ids, expert_ids,
+                                    n_padded, block_m, act, post_norm_w, out, &L);
+  if (rc != MOE_OK || M == 0) return rc;
+  WsPlan w;
+  if (!plan_workspace(L, M, top_k, block_m, &w, kNoAllocSplitBudget)) return MOE_ERR_CUDA;
+  if (w.total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
+  void* scratch = noalloc_scratch();
+  if (!scratch) return MOE_ERR_CUDA;
+  return forward_impl(desc, L, w, packed, x, M, top_k, topk_ids, topk_weights, expert_base, sorted_ids, expert_ids,
+                      n_padded, block_m, act, alpha, limit, routed_scaling_factor, post_norm_w, norm_eps, out,
+                      scratch, stream);
 }
 
 extern "C" int moe_set_trace_events(void* const* events, int n) {
