@@ -82,8 +82,9 @@ def test_rejects_bad_arguments_without_device(lib):
 
 def test_block_m_chooser(lib):
     d = lib.moe_layer_desc(0, 128, 4096, 1536, 128, 0, 0, 0)
-    assert lib.moe_choose_block_m(d, 1, 8, 128) == 16
-    assert lib.moe_choose_block_m(d, 16, 8, 128) == 16
+    assert lib.moe_choose_block_m(d, 1, 8, 128) == 8
+    assert lib.moe_choose_block_m(d, 16, 8, 128) == 8
+    assert lib.moe_choose_block_m(d, 256, 8, 128) == 16
     assert lib.moe_choose_block_m(d, 4096, 8, 128) == 128
     # monotone in the token count
     prev = 0

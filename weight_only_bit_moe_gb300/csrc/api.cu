@@ -78,14 +78,17 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   return true;
 }
 
-cudaError_t launch_gemm(int fmt, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
+cudaError_t launch_gemm(int fmt, bool small, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
   switch (fmt) {
-    case MOE_W_INT4_U4B8: return launch_gemm_int4(gated, bn, g, grid, st);
-    case MOE_W_MXFP4: return launch_gemm_mxfp4(gated, bn, g, grid, st);
-    case MOE_W_NVFP4: return launch_gemm_nvfp4(gated, bn, g, grid, st);
+    case MOE_W_INT4_U4B8: return launch_gemm_int4(small, gated, bn, g, grid, st);
+    case MOE_W_MXFP4: return launch_gemm_mxfp4(small, gated, bn, g, grid, st);
+    case MOE_W_NVFP4: return launch_gemm_nvfp4(small, gated, bn, g, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
+
+// Token blocks up to this size run on the register-fed kernel.
+constexpr int kSmallBlockMax = 32;
 
 bool valid_block_m(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128; }
 
@@ -117,6 +120,21 @@ bool make_act_map(CUtensorMap* m, const void* base, bool f16, int64_t cols, int6
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same matrix viewed as [rows][cols / 64][64]: dims (64, rows, cols / 64),
+// boxes of 64 x box_rows x box_stages landing as [stage][row][64] with the
+// 128-byte swizzle, so one copy brings several 64-column stages.
+bool make_act_map3(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int box_rows, int box_stages) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || cols % 64) return false;
+  const cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128u};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_stages};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaEvent_t g_trace[4] = {nullptr, nullptr, nullptr, nullptr};
 bool g_tracing = false;
 
@@ -132,6 +150,7 @@ extern "C" int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, 
   if (!desc || M < 0 || top_k <= 0 || num_routed_ids <= 0) return MOE_ERR_INVALID;
   // expected rows per local expert: routed pairs spread over the routed id range
   const double rows = (double)M * top_k / (double)num_routed_ids;
+  if (rows <= 8.0) return 8;
   if (rows <= 16.0) return 16;
   if (rows <= 32.0) return 32;
   if (rows <= 96.0) return 64;
@@ -176,13 +195,19 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
-  const int bn = block_m < 16 ? 16 : block_m;
+  const bool small = block_m <= kSmallBlockMax;
+  const int bn = block_m;  // token columns per tile
 
   GemmArgs g{};
   // GEMM1 reads the gathered fp16 rows; GEMM2 GEMM1's fp16 output
-  if (!make_act_map(&g.tmap_b, ws + w.xs_off, true, L.K, w.cap, bn)) return MOE_ERR_CUDA;
   CUtensorMap map2;
-  if (!make_act_map(&map2, ws + w.a_off, true, L.Npad, w.cap, bn)) return MOE_ERR_CUDA;
+  if (small) {
+    if (!make_act_map3(&g.tmap_b, ws + w.xs_off, L.K, w.cap, bn, kSmallChunk)) return MOE_ERR_CUDA;
+    if (!make_act_map3(&map2, ws + w.a_off, L.Npad, w.cap, bn, kSmallChunk)) return MOE_ERR_CUDA;
+  } else {
+    if (!make_act_map(&g.tmap_b, ws + w.xs_off, true, L.K, w.cap, bn)) return MOE_ERR_CUDA;
+    if (!make_act_map(&map2, ws + w.a_off, true, L.Npad, w.cap, bn)) return MOE_ERR_CUDA;
+  }
 
   // prologue: status word and split-K counters to zero, routed rows gathered
   PrepArgs pa{};
@@ -220,7 +245,7 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.split_rows = w.rows1;
   g.partial = reinterpret_cast<float*>(ws + w.part1_off);
   g.counters = reinterpret_cast<int32_t*>(ws + w.counters1_off);
-  if (launch_gemm(L.fmt, true, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(L.fmt, small, true, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(1, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2
@@ -230,7 +255,7 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.split_rows = w.rows2;
   g.partial = reinterpret_cast<float*>(ws + w.part2_off);
   g.counters = reinterpret_cast<int32_t*>(ws + w.counters2_off);
-  if (launch_gemm(L.fmt, false, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(L.fmt, small, false, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(2, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   // combine

@@ -23,12 +23,18 @@ namespace moe {
 // _pad_w13/_pad_w2 tile padding); padded codes decode to 0.
 //
 // Each tile is a sequence of K-stages of 64 reduction elements.  A stage's
-// packed codes are 8 KiB: uint4 units [j][r] (j = 0,1 is the 32-element half of
-// the stage, r the tile row), so that thread r of the dequant warps reads
-// units r and 256 + r, both conflict-free.  Inside one 32-bit word (8 elements
-// e0..e7 of a row): INT4 puts element 2i at bits 4i and element 2i+1 at bits
-// 16+4i (a mask yields an f16x2 pair of consecutive elements); FP4 keeps element
-// order, two codes per byte, for the hardware E2M1x2 -> f16x2 conversion.
+// packed codes are 8 KiB: uint4 units [j][r] (j = 0,1, r the tile row), so
+// that a thread that owns row r reads units r and 256 + r, both
+// conflict-free.  A row's 64 codes in a stage are eight 32-bit words v = 2t + h
+// (word v is word v % 4 of unit v / 4), each holding four pairs of consecutive
+// reduction elements: pair p of word (t, h) starts at k = 32h + 2t + 8p.  This
+// is the register fragment of the m16n8k16 tensor-core instruction: fragment
+// lane t of a row finds the pairs it needs for the stage's four 16-element
+// K-steps -- (2t, 2t+1) and (2t+8, 2t+9) of each -- in words (t, 0) and (t, 1),
+// one 8-byte load.  Inside a word, INT4 puts the first element of pair p at
+// bits 4p and the second at bits 16+4p (a mask yields an f16x2 pair); FP4 puts
+// pair p in byte p, first element in the low nibble, for the hardware
+// E2M1x2 -> f16x2 conversion.
 //
 // Scales ride in front of the stage that first needs them: INT4 (one bf16 per
 // 128 = two stages) only in front of even stages, 256 x bf16; MXFP4 two E8M0
@@ -336,6 +342,28 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// ---------------------------------------------------------------- register-fed tensor cores
+// D (16 x 8, fp32) += A (16 x 16, fp16, row-major fragment) * B (16 x 8, fp16).
+// Fragment of lane (g = lane / 4, t = lane % 4): a0 = A[g][2t..2t+1],
+// a1 = A[g+8][2t..2t+1], a2 = A[g][2t+8..2t+9], a3 = A[g+8][2t+8..2t+9];
+// b0 = B[2t..2t+1][g], b1 = B[2t+8..2t+9][g]; d0, d1 = D[g][2t..2t+1],
+// d2, d3 = D[g+8][2t..2t+1].
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Four 8 x 8 16-bit matrices from shared memory; lane l gives the address of
+// row l % 8 of matrix l / 8 and receives row l / 4, columns 2(l % 4)..+1 of each.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- bf16 bits
 __device__ __forceinline__ uint32_t bf162_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 __device__ __forceinline__ __nv_bfloat162 bits_bf162(uint32_t u) { return *reinterpret_cast<__nv_bfloat162*>(&u); }
@@ -353,8 +381,8 @@ __device__ __forceinline__ float round_bf16(float f) { return __bfloat162float(_
 // produced as value * scale * 2^-8 (kFp4Unscale restores the 2^8 in the fp32
 // epilogue), which keeps large block scales inside the fp16 range.
 
-// 8 INT4 (uint4b8) codes of one word -> 4 f16x2, elements in order.  Word
-// layout from the repack: element 2i at bits 4i, element 2i+1 at bits 16 + 4i.
+// 8 INT4 (uint4b8) codes of one word -> its 4 pairs as f16x2.  Word layout from
+// the repack: pair p has its first element at bits 4p, its second at 16 + 4p.
 // Pairs 0 and 2 are (1024 + q) - 1032; pairs 1 and 3 sit 4 bits higher and
 // are (1024 + 16q) - 1152 = 16(q - 8), scaled by s / 16.
 __device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t s2, uint32_t s2_16, uint32_t (&o)[4]) {
@@ -372,8 +400,9 @@ __device__ __forceinline__ void int4x8_f16(uint32_t w, uint32_t s2, uint32_t s2_
   }
 }
 
-// 8 E2M1 codes of one word (byte i = element 2i low nibble, 2i+1 high nibble)
-// -> 4 f16x2 with the hardware conversion, each times its multiplier pair.
+// 8 E2M1 codes of one word (byte p = pair p, first element in the low nibble)
+// -> 4 f16x2 with the hardware conversion; pairs 0, 1 times m01, pairs 2, 3
+// times m23.
 __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t m01, uint32_t m23, uint32_t (&o)[4]) {
   uint32_t v[4];
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"

@@ -333,15 +333,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[ps]);
         const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t o[32];
+        uint32_t o[32];  // TMEM column c = K pair (2c, 2c+1) of the stage
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int v = 0; v < 8; ++v) {
+          // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
+          // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
+          const int t = v >> 1, h = v & 1;
           uint32_t t4[4];
-          if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[i], m[0], m[1], t4);
-          else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[i], m[i >> 2], m[i >> 2], t4);
-          else e2m1x8_f16(wd[i], m[i >> 1], m[i >> 1], t4);
+          if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[0], m[1], t4);
+          else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[h], m[h], t4);
+          else e2m1x8_f16(wd[v], m[2 * h], m[2 * h + 1], t4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) o[4 * i + k] = t4[k];
+          for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
         }
         mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
         tc_fence_after();

@@ -1,0 +1,500 @@
+// Grouped W4A16 GEMM for small token blocks (block_m = 8, 16 or 32): the
+// decode and small-batch shapes, where every routed expert's weights are
+// streamed from HBM once per token block and the layer is bound by HBM
+// bandwidth, not by tensor math.
+//
+// Same function as moe_gemm_kernel (gemm.cuh) -- GEMM1 with the fused gated
+// activation, or GEMM2 -- on the same packed layout, built for a different
+// bottleneck:
+//
+//   * weights reach registers, never tensor memory: eight consumer warps each
+//     own 32 rows of the 256-row tile, load their 4-bit codes from the staged
+//     chunk (one 8-byte load per row and stage, in the register-fragment order
+//     the repack writes), dequantise them in registers to fp16 and feed them
+//     as the A operand of m16n8k16 tensor-core instructions; tokens are the
+//     8-wide N side.  At 8..32 tokens a 64-K stage costs 128..512 tensor
+//     cycles per SM, under the ~380 cycles HBM needs to deliver it, and no
+//     cross-warp handoff sits between dequantisation and the MMA;
+//   * GEMM1 pairs gate and up rows inside each 16-row fragment (rows 0..7 gate
+//     features, rows 8..15 the same up features), so the activation is applied
+//     in the registers that hold both accumulators;
+//   * one producer thread streams 4-stage chunks (~34 KB of packed codes and
+//     scales in one bulk copy, plus the block's activation rows for those
+//     stages in one 3-D TMA tile) into a 4..6-deep ring; large copies keep a
+//     single issuing thread at HBM speed;
+//   * the persistent grid, the work order (tile fastest) and the device-side
+//     split-K with last-arrival reduction in split order are those of
+//     moe_gemm_kernel; the split is chosen at period granularity.
+#pragma once
+
+#include <cuda.h>
+
+#include "gemm.cuh"
+
+namespace moe {
+
+constexpr int kSmallChunk = 4;  // 64-K stages per TMA chunk
+constexpr int kSmallConsumerWarps = 8;
+constexpr int kSmallThreads = (1 + kSmallConsumerWarps) * 32;
+constexpr int kSmallWBytes = kSmallChunk * (kPackedStageBytes + 1024);  // codes + largest scale block
+
+template <int BN>
+struct SmallSmem {
+  static constexpr int kBBytes = kSmallChunk * BN * 128;  // activation rows of a chunk, [stage][row][64]
+  static constexpr int kSlotBytes = kSmallWBytes + kBBytes;
+  static constexpr int kFit = (kSmemBudget - 2048) / kSlotBytes;
+  static constexpr int kSlots = kFit > 6 ? 6 : kFit;
+  static constexpr int kBar = kSlots * kSlotBytes;
+  static constexpr int kMisc = kBar + 2 * kSlots * 8;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kSlots >= 4, "ring too shallow");
+  static_assert(kAlloc <= 232448, "shared memory over the per-CTA limit");
+  static_assert(kBBytes % 1024 == 0 && kSmallWBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+};
+
+// Split-K choice in units of 1/8 stage: each wave streams ceil(units/S)
+// scale periods; a split item also writes its fp32 partial (256 rows x BN x 4 B
+// = BN/8 stages) and the last CTA of each item reads S of them back.
+__device__ __forceinline__ WorkPlan make_plan_small(const GemmArgs& g, bool gated, int bn) {
+  WorkPlan p;
+  p.nb = *g.n_padded / g.block_m;
+  p.T = gated ? g.L.T1 : g.L.T2;
+  const int stages = gated ? g.L.S1 : g.L.S2;
+  p.units = stages / g.L.period;
+  const int base = p.T * p.nb;
+  const int grid = (int)gridDim.x;
+  int S = 1;
+  if (base > 0 && base < grid && p.nb * g.block_m <= g.split_rows) {
+    const int per = g.L.period * 8;
+    int best = p.units * per;
+    const int smax = min(g.max_split, p.units);
+    for (int s = 2; s <= smax; ++s) {
+      const int waves = (base * s + grid - 1) / grid;
+      const int cost = waves * (((p.units + s - 1) / s) * per + bn) + s * bn;
+      if (cost < best) { best = cost; S = s; }
+    }
+  }
+  p.S = S;
+  p.items = base * S;
+  return p;
+}
+
+// TMA: a 3-D tile (box from the tensor map) at (c0, c1, c2).
+__device__ __forceinline__ void tma_tile3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Compile-time view of one format's packed stages (the Layout fields period,
+// scale_bytes and period_bytes as constants): stage ss of a chunk that starts
+// on a scale period begins at stage_off(ss); its codes at codes_off(ss).
+template <int FMT>
+struct PackedFmt {
+  static constexpr int kPeriod = FMT == MOE_W_INT4_U4B8 ? 2 : 1;
+  static constexpr int kScaleBytes = kTileRows * (FMT == MOE_W_NVFP4 ? 4 : 2);
+  static constexpr int kPeriodBytes = kScaleBytes + kPeriod * kPackedStageBytes;
+  __host__ __device__ static constexpr int stage_off(int ss) {
+    return (ss / kPeriod) * kPeriodBytes + (ss % kPeriod ? kScaleBytes + (ss % kPeriod) * kPackedStageBytes : 0);
+  }
+  __host__ __device__ static constexpr int codes_off(int ss) { return (ss / kPeriod) * kPeriodBytes + kScaleBytes + (ss % kPeriod) * kPackedStageBytes; }
+};
+
+// 8 INT4 (uint4b8) codes of one word -> its 4 pairs of (q - 8) as f16x2, exact:
+// pairs 0 and 2 are (1024 + q) - 1032, pairs 1 and 3 (1024 + 16q) / 16 - 72.
+__device__ __forceinline__ void int4x8_f16_unscaled(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t t[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x64006400u,
+                         (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x64006400u};
+  const __half2 c1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 r16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
+  const __half2 cm72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));  // -72
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 x = *reinterpret_cast<const __half2*>(&t[i]);
+    const __half2 r = (i & 1) ? __hfma2(x, r16, cm72) : __hsub2(x, c1032);
+    o[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+// f16x2 multipliers of one FP4 row for the stage's scale block: MXFP4 one per
+// 32 K (m[0], m[1]), NVFP4 one per 16 K (m[0..3]).
+template <int FMT>
+__device__ __forceinline__ void fp4_row_multipliers(const unsigned char* scales, int row, uint32_t (&m)[4]) {
+  if (FMT == MOE_W_MXFP4) {
+    const uint32_t sv = reinterpret_cast<const uint16_t*>(scales)[row];
+    const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
+    m[0] = a | (a << 16);
+    m[1] = c | (c << 16);
+  } else {
+    const uint32_t sv = reinterpret_cast<const uint32_t*>(scales)[row];
+    const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
+    m[0] = __byte_perm(lo, 0, 0x1010);
+    m[1] = __byte_perm(lo, 0, 0x3232);
+    m[2] = __byte_perm(hi, 0, 0x1010);
+    m[3] = __byte_perm(hi, 0, 0x3232);
+  }
+}
+
+// Per-warp state of the consumer loop.
+template <int NT>
+struct SmallFrag {
+  int rows[2][2];           // tile rows: row gq + 8h of 16-row fragment i
+  uint32_t code_off[2][2];  // this lane's 8 bytes of each row inside a stage's code block
+  uint32_t b_row[NT > 1 ? NT / 2 : 1];
+  uint32_t b_sel;
+};
+
+// Activation fragments of stage block sb ([BN][64] fp16, 128-byte swizzle:
+// 16-byte chunk c of token row n at n * 128 + ((c ^ (n & 7)) << 4)):
+// bf[step][n-tile][0..1].
+template <int NT>
+__device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT>& F, uint32_t (&bf)[4][NT][2]) {
+  if (NT == 1) {
+#pragma unroll
+    for (int j0 = 0; j0 < 4; j0 += 2) {
+      const uint32_t c = (uint32_t)(2 * j0) + F.b_sel;
+      ldmatrix_x4(sb + F.b_row[0] * 128 + ((c ^ (F.b_row[0] & 7)) << 4), bf[j0][0][0], bf[j0][0][1],
+                  bf[j0 + 1][0][0], bf[j0 + 1][0][1]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t c = (uint32_t)(2 * j) + F.b_sel;
+#pragma unroll
+      for (int q = 0; q < (NT > 1 ? NT / 2 : 1); ++q)
+        ldmatrix_x4(sb + F.b_row[q] * 128 + ((c ^ (F.b_row[q] & 7)) << 4), bf[j][2 * q][0], bf[j][2 * q][1],
+                    bf[j][2 * q + 1][0], bf[j][2 * q + 1][1]);
+    }
+  }
+}
+
+// NST stages of a chunk (starting on a scale period) into the accumulators.
+// INT4 keeps each 128-K group's sum of (q - 8) * x in its own accumulators and
+// adds it times the group's fp32 scale; FP4 scales the codes in fp16 (exact).
+template <int FMT, int NT, int BN, int NST>
+__device__ __forceinline__ void consume_chunk(const unsigned char* wsl, uint32_t bsl, const SmallFrag<NT>& F,
+                                              float (&acc)[2][NT][4], uint32_t (&m)[2][2][4]) {
+  using PF = PackedFmt<FMT>;
+  if constexpr (FMT == MOE_W_INT4_U4B8) {
+#pragma unroll
+    for (int gp = 0; gp < NST / 2; ++gp) {
+      float sc[2][2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          sc[i][h] = bf16_bits_to_float(reinterpret_cast<const uint16_t*>(wsl + PF::stage_off(2 * gp))[F.rows[i][h]]);
+      float part[2][NT][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) part[i][n][c] = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int ss = 2 * gp + s2;
+        const unsigned char* codes = wsl + PF::codes_off(ss);
+        uint2 wv[2][2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) wv[i][h] = *reinterpret_cast<const uint2*>(codes + F.code_off[i][h]);
+        uint32_t bf[4][NT][2];
+        load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t p0[4], p1[4];  // fragment rows gq and gq + 8
+            int4x8_f16_unscaled(h ? wv[i][0].y : wv[i][0].x, p0);
+            int4x8_f16_unscaled(h ? wv[i][1].y : wv[i][1].x, p1);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              mma_16816(part[i][n], p0[0], p1[0], p0[1], p1[1], bf[2 * h][n][0], bf[2 * h][n][1]);
+              mma_16816(part[i][n], p0[2], p1[2], p0[3], p1[3], bf[2 * h + 1][n][0], bf[2 * h + 1][n][1]);
+            }
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[i][n][c] = fmaf(sc[i][c >> 1], part[i][n][c], acc[i][n][c]);
+    }
+  } else {
+#pragma unroll
+    for (int ss = 0; ss < NST; ++ss) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) fp4_row_multipliers<FMT>(wsl + PF::stage_off(ss), F.rows[i][h], m[i][h]);
+      const unsigned char* codes = wsl + PF::codes_off(ss);
+      uint2 wv[2][2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) wv[i][h] = *reinterpret_cast<const uint2*>(codes + F.code_off[i][h]);
+      uint32_t bf[4][NT][2];
+      load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t p0[4], p1[4];
+          if (FMT == MOE_W_MXFP4) {
+            e2m1x8_f16(h ? wv[i][0].y : wv[i][0].x, m[i][0][h], m[i][0][h], p0);
+            e2m1x8_f16(h ? wv[i][1].y : wv[i][1].x, m[i][1][h], m[i][1][h], p1);
+          } else {
+            e2m1x8_f16(h ? wv[i][0].y : wv[i][0].x, m[i][0][2 * h], m[i][0][2 * h + 1], p0);
+            e2m1x8_f16(h ? wv[i][1].y : wv[i][1].x, m[i][1][2 * h], m[i][1][2 * h + 1], p1);
+          }
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            mma_16816(acc[i][n], p0[0], p1[0], p0[1], p1[1], bf[2 * h][n][0], bf[2 * h][n][1]);
+            mma_16816(acc[i][n], p0[2], p1[2], p0[3], p1[3], bf[2 * h + 1][n][0], bf[2 * h + 1][n][1]);
+          }
+        }
+    }
+  }
+}
+
+template <int FMT, bool GATED, int BN>
+__global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const __grid_constant__ GemmArgs g) {
+  using SM = SmallSmem<BN>;
+  constexpr int kSlots = SM::kSlots;
+  constexpr int NT = BN / 8;  // 8-token column tiles
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
+  uint64_t* empty = full + kSlots;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + SM::kMisc);  // [1] abort, [2] last-arrival flag
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[1]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Layout& L = g.L;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kSmallConsumerWarps);
+    }
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g.tmap_b)) : "memory");
+  __syncthreads();
+
+  const WorkPlan plan = make_plan_small(g, GATED, BN);
+  const int64_t tile_bytes = GATED ? L.tile1_bytes : L.tile2_bytes;
+  const uint8_t* wbase = g.packed + (GATED ? L.w13_off : L.w2_off);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t ck = 0;
+      for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
+        int b, tile, split, s0, s1;
+        decode_item(plan, w, b, tile, split);
+        stage_range(plan, L, split, s0, s1);
+        const int e = g.expert_ids[b];
+        const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
+        for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
+          const int c1 = min(c0 + kSmallChunk, s1);
+          const int slot = ck % kSlots;
+          mbar_wait(&empty[slot], ((ck / kSlots) + 1) & 1, abort_flag, g.status);
+          const int64_t off0 = stage_offset(L, c0);
+          const uint32_t wbytes = (uint32_t)(stage_offset(L, c1) - off0);
+          unsigned char* dst = smem + slot * SM::kSlotBytes;
+          mbar_arrive_expect_tx(&full[slot], wbytes + SM::kBBytes);
+          bulk_g2s(dst, tb + off0, wbytes, &full[slot], pol);
+          tma_tile3d(smem_u32(dst + kSmallWBytes), &g.tmap_b, 0, b * g.block_m, c0, &full[slot]);
+        }
+      }
+      // leave no copy in flight
+      for (uint32_t i = 0; i < (uint32_t)kSlots && i < ck; ++i) {
+        const uint32_t k = ck - 1 - i;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&full[k % kSlots], (k / kSlots) & 1) && global_timer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const int cw = warp - 1;
+    const int gq = lane >> 2, tq = lane & 3;
+    SmallFrag<NT> F;
+    int (&rows)[2][2] = F.rows;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (GATED) {  // gate feature f in fragment row gq, its up row in gq + 8
+        rows[i][0] = 16 * cw + 8 * i + gq;
+        rows[i][1] = 128 + rows[i][0];
+      } else {
+        rows[i][0] = 32 * cw + 16 * i + gq;
+        rows[i][1] = rows[i][0] + 8;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) F.code_off[i][h] = (uint32_t)(((tq >> 1) * 256 + rows[i][h]) * 16 + (tq & 1) * 8);
+    if (NT == 1) {
+      F.b_row[0] = (uint32_t)(lane & 7);
+      F.b_sel = (uint32_t)(lane >> 3);  // chunk offset 0..3 (two K-steps per load)
+    } else {
+#pragma unroll
+      for (int q = 0; q < (NT > 1 ? NT / 2 : 1); ++q) F.b_row[q] = (uint32_t)(16 * q + (lane & 7) + 8 * (lane >> 4));
+      F.b_sel = (uint32_t)((lane >> 3) & 1);
+    }
+    const float* gs_tab = reinterpret_cast<const float*>(g.packed + (GATED ? L.gs13_off : L.gs2_off));
+    const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (GATED ? L.b13_off : L.b2_off));
+    const int Npad = L.Npad;
+    const int width = GATED ? 2 * Npad : L.K;
+    uint32_t m[2][2][4] = {};
+    uint32_t ck = 0;
+
+    for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
+      int b, tile, split, s0, s1;
+      decode_item(plan, w, b, tile, split);
+      stage_range(plan, L, split, s0, s1);
+      const int e = g.expert_ids[b];
+      float acc[2][NT][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+
+      for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
+        const int slot = ck % kSlots;
+        mbar_wait(&full[slot], (ck / kSlots) & 1, abort_flag, g.status);
+        const unsigned char* wsl = smem + slot * SM::kSlotBytes;
+        const uint32_t bsl = smem_u32(wsl + kSmallWBytes);
+        const int nst = min(kSmallChunk, s1 - c0);
+        if (nst == 4) consume_chunk<FMT, NT, BN, 4>(wsl, bsl, F, acc, m);
+        else if (nst == 2) consume_chunk<FMT, NT, BN, 2>(wsl, bsl, F, acc, m);
+        else if (FMT != MOE_W_INT4_U4B8) {  // INT4 chunks always hold whole 2-stage periods
+          if (nst == 3) consume_chunk<FMT, NT, BN, 3>(wsl, bsl, F, acc, m);
+          else consume_chunk<FMT, NT, BN, 1>(wsl, bsl, F, acc, m);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+
+      // ---------------------------------------------------------- epilogue
+      if (plan.S > 1) {
+        // store this slice's fp32 partial, rows by sorted position
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int pos = b * g.block_m + n * 8 + 2 * tq + c;
+              float* dst = g.partial + ((int64_t)split * g.split_rows + pos) * width;
+              if (GATED) {
+                const int f = tile * 128 + 16 * cw + 8 * i + gq;
+                __stcg(dst + f, acc[i][n][c]);
+                __stcg(dst + Npad + f, acc[i][n][2 + c]);
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int o = tile * 256 + rows[i][h];
+                  if (o < L.K) __stcg(dst + o, acc[i][n][2 * h + c]);
+                }
+              }
+            }
+        __threadfence();
+        named_bar_sync(1, kSmallConsumerWarps * 32);
+        if (cw == 0 && lane == 0) {
+          const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[b * plan.T + tile]),
+                                         (unsigned)(plan.S - 1));
+          misc[2] = old == (unsigned)(plan.S - 1) ? 1u : 0u;
+        }
+        named_bar_sync(1, kSmallConsumerWarps * 32);
+        const bool last = misc[2] != 0;
+        named_bar_sync(1, kSmallConsumerWarps * 32);  // misc[2] is read before the next item rewrites it
+        if (!last) continue;
+        __threadfence();
+        // sum all slices in split order
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+        for (int sp = 0; sp < plan.S; ++sp)
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int pos = b * g.block_m + n * 8 + 2 * tq + c;
+                const float* src = g.partial + ((int64_t)sp * g.split_rows + pos) * width;
+                if (GATED) {
+                  const int f = tile * 128 + 16 * cw + 8 * i + gq;
+                  acc[i][n][c] += __ldcg(src + f);
+                  acc[i][n][2 + c] += __ldcg(src + Npad + f);
+                } else {
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    const int o = tile * 256 + rows[i][h];
+                    if (o < L.K) acc[i][n][2 * h + c] += __ldcg(src + o);
+                  }
+                }
+              }
+      }
+      const float gsc = gs_tab[e];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (GATED) {
+          const int f = tile * 128 + 16 * cw + 8 * i + gq;
+          float bg = 0.f, bu = 0.f;
+          if (g.has_bias) {
+            bg = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + f]);
+            bu = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + Npad + f]);
+          }
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int pos = b * g.block_m + n * 8 + 2 * tq + c;
+              const int sid = g.sorted_ids[pos];
+              const float hg = acc[i][n][c] * gsc + bg;
+              const float hu = acc[i][n][2 + c] * gsc + bu;
+              const float a = sid < g.pairs ? act_fn(g.act_kind, hg, hu, g.alpha, g.limit) : 0.0f;
+              g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
+            }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int o = tile * 256 + rows[i][h];
+            if (o >= L.K) continue;
+            const float bo = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + o]) : 0.f;
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int pos = b * g.block_m + n * 8 + 2 * tq + c;
+                const int sid = g.sorted_ids[pos];
+                if (sid < g.pairs) g.y_out[(int64_t)sid * L.K + o] = acc[i][n][2 * h + c] * gsc + bo;
+              }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace moe

@@ -63,21 +63,25 @@ __global__ void repack_codes_kernel(RepackArgs a, int which) {
     uint32_t words[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
+      // word v = 2t + h of the row's stage holds pairs starting at 32h + 2t + 8p
+      const int v = 4 * j + w, t = v >> 1, h = v & 1;
       uint32_t word = 0;
 #pragma unroll
-      for (int el = 0; el < 8; ++el) {
-        const int k = s * kStageK + 32 * j + 8 * w + el;
-        uint32_t q = zero_code(L.fmt);
-        if (srow && k < red) {
-          const uint8_t b = srow[k >> 1];
-          q = (k & 1) ? (b >> 4) : (b & 15u);
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int k = s * kStageK + 32 * h + 2 * t + 8 * p + e2;
+          uint32_t q = zero_code(L.fmt);
+          if (srow && k < red) {
+            const uint8_t b = srow[k >> 1];
+            q = (k & 1) ? (b >> 4) : (b & 15u);
+          }
+          // INT4: first element of pair p at bits 4p, second at 16 + 4p (mask-and-magic
+          // pairs); FP4: pair p in byte p, first element in the low nibble, as the
+          // hardware E2M1x2 conversion reads them
+          const int pos = L.fmt == MOE_W_INT4_U4B8 ? (e2 ? 16 + 4 * p : 4 * p) : 8 * p + 4 * e2;
+          word |= q << pos;
         }
-        // INT4: element 2i at bits 4i, 2i+1 at bits 16 + 4i (mask-and-magic pairs);
-        // FP4: element order, byte i = elements 2i (low nibble), 2i+1 (high), as the
-        // hardware E2M1x2 conversion reads them
-        const int pos = L.fmt == MOE_W_INT4_U4B8 ? ((el & 1) ? 16 + 4 * (el >> 1) : 4 * (el >> 1)) : 4 * el;
-        word |= q << pos;
-      }
       words[w] = word;
     }
     uint8_t* dst = a.out + (which ? L.w2_off : L.w13_off) + ((int64_t)e * T + tile) * tile_bytes +
