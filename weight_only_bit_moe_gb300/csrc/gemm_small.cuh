@@ -35,6 +35,7 @@ namespace moe {
 
 constexpr int kSmallChunk = 4;  // 64-K stages per TMA chunk
 constexpr int kSmallConsumerWarps = 8;
+constexpr int kSmallMI = kTileRows / 16 / kSmallConsumerWarps;  // 16-row fragments per consumer warp
 constexpr int kSmallThreads = (1 + kSmallConsumerWarps) * 32;
 constexpr int kSmallWBytes = kSmallChunk * (kPackedStageBytes + 1024);  // codes + largest scale block
 
@@ -121,17 +122,33 @@ __device__ __forceinline__ void int4x8_f16_unscaled(uint32_t w, uint32_t (&o)[4]
   }
 }
 
-// f16x2 multipliers of one FP4 row for the stage's scale block: MXFP4 one per
-// 32 K (m[0], m[1]), NVFP4 one per 16 K (m[0..3]).
+// Shared-memory loads through 32-bit shared addresses (ordered after the
+// barrier waits like every other volatile access).
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// f16x2 multipliers of one FP4 row from its scale bytes: MXFP4 one per 32 K
+// (m[0], m[1]), NVFP4 one per 16 K (m[0..3]).
 template <int FMT>
-__device__ __forceinline__ void fp4_row_multipliers(const unsigned char* scales, int row, uint32_t (&m)[4]) {
+__device__ __forceinline__ void fp4_row_multipliers(uint32_t sv, uint32_t (&m)[4]) {
   if (FMT == MOE_W_MXFP4) {
-    const uint32_t sv = reinterpret_cast<const uint16_t*>(scales)[row];
-    const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
+    const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16((sv >> 8) & 0xFF);
     m[0] = a | (a << 16);
     m[1] = c | (c << 16);
   } else {
-    const uint32_t sv = reinterpret_cast<const uint32_t*>(scales)[row];
     const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
     m[0] = __byte_perm(lo, 0, 0x1010);
     m[1] = __byte_perm(lo, 0, 0x3232);
@@ -140,58 +157,52 @@ __device__ __forceinline__ void fp4_row_multipliers(const unsigned char* scales,
   }
 }
 
-// Per-warp state of the consumer loop.
+// Per-warp constants of the consumer loop (byte offsets inside a slot).
 template <int NT>
 struct SmallFrag {
-  int rows[2][2];           // tile rows: row gq + 8h of 16-row fragment i
-  uint32_t code_off[2][2];  // this lane's 8 bytes of each row inside a stage's code block
-  uint32_t b_row[NT > 1 ? NT / 2 : 1];
-  uint32_t b_sel;
+  static constexpr int NQ = NT > 1 ? NT / 2 : 1;
+  int rows[kSmallMI][2];           // tile rows: row gq + 8h of 16-row fragment i
+  uint32_t code_off[kSmallMI][2];  // this lane's 8 bytes of each row inside a stage's code block
+  uint32_t sc_off[kSmallMI][2];    // each row's scale inside a scale block
+  uint32_t b_off[4][NQ];           // ldmatrix row address of K-step j (token group q) in a stage block
 };
 
-// Activation fragments of stage block sb ([BN][64] fp16, 128-byte swizzle:
-// 16-byte chunk c of token row n at n * 128 + ((c ^ (n & 7)) << 4)):
+// Activation fragments of one stage block ([BN][64] fp16, 128-byte swizzle):
 // bf[step][n-tile][0..1].
 template <int NT>
 __device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT>& F, uint32_t (&bf)[4][NT][2]) {
   if (NT == 1) {
 #pragma unroll
-    for (int j0 = 0; j0 < 4; j0 += 2) {
-      const uint32_t c = (uint32_t)(2 * j0) + F.b_sel;
-      ldmatrix_x4(sb + F.b_row[0] * 128 + ((c ^ (F.b_row[0] & 7)) << 4), bf[j0][0][0], bf[j0][0][1],
-                  bf[j0 + 1][0][0], bf[j0 + 1][0][1]);
-    }
+    for (int j0 = 0; j0 < 4; j0 += 2)
+      ldmatrix_x4(sb + F.b_off[j0][0], bf[j0][0][0], bf[j0][0][1], bf[j0 + 1][0][0], bf[j0 + 1][0][1]);
   } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t c = (uint32_t)(2 * j) + F.b_sel;
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int q = 0; q < (NT > 1 ? NT / 2 : 1); ++q)
-        ldmatrix_x4(sb + F.b_row[q] * 128 + ((c ^ (F.b_row[q] & 7)) << 4), bf[j][2 * q][0], bf[j][2 * q][1],
-                    bf[j][2 * q + 1][0], bf[j][2 * q + 1][1]);
-    }
+      for (int q = 0; q < SmallFrag<NT>::NQ; ++q)
+        ldmatrix_x4(sb + F.b_off[j][q], bf[j][2 * q][0], bf[j][2 * q][1], bf[j][2 * q + 1][0], bf[j][2 * q + 1][1]);
   }
 }
 
-// NST stages of a chunk (starting on a scale period) into the accumulators.
-// INT4 keeps each 128-K group's sum of (q - 8) * x in its own accumulators and
-// adds it times the group's fp32 scale; FP4 scales the codes in fp16 (exact).
+// NST stages of a chunk (starting on a scale period; wsl its shared address)
+// into the accumulators.  INT4 keeps each 128-K group's sum of (q - 8) * x in
+// its own accumulators and adds it times the group's fp32 scale; FP4 scales the
+// codes in fp16 (exact).
 template <int FMT, int NT, int BN, int NST>
-__device__ __forceinline__ void consume_chunk(const unsigned char* wsl, uint32_t bsl, const SmallFrag<NT>& F,
-                                              float (&acc)[2][NT][4], uint32_t (&m)[2][2][4]) {
+__device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const SmallFrag<NT>& F,
+                                              float (&acc)[kSmallMI][NT][4], uint32_t (&m)[kSmallMI][2][4]) {
   using PF = PackedFmt<FMT>;
   if constexpr (FMT == MOE_W_INT4_U4B8) {
 #pragma unroll
     for (int gp = 0; gp < NST / 2; ++gp) {
-      float sc[2][2];
+      float sc[kSmallMI][2];
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          sc[i][h] = bf16_bits_to_float(reinterpret_cast<const uint16_t*>(wsl + PF::stage_off(2 * gp))[F.rows[i][h]]);
-      float part[2][NT][4];
+        for (int h = 0; h < 2; ++h) sc[i][h] = __uint_as_float(lds16(wsl + PF::stage_off(2 * gp) + F.sc_off[i][h]) << 16);
+      float part[kSmallMI][NT][4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -199,16 +210,15 @@ __device__ __forceinline__ void consume_chunk(const unsigned char* wsl, uint32_t
 #pragma unroll
       for (int s2 = 0; s2 < 2; ++s2) {
         const int ss = 2 * gp + s2;
-        const unsigned char* codes = wsl + PF::codes_off(ss);
-        uint2 wv[2][2];
+        uint2 wv[kSmallMI][2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
-          for (int h = 0; h < 2; ++h) wv[i][h] = *reinterpret_cast<const uint2*>(codes + F.code_off[i][h]);
+          for (int h = 0; h < 2; ++h) wv[i][h] = lds64(wsl + PF::codes_off(ss) + F.code_off[i][h]);
         uint32_t bf[4][NT][2];
         load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t p0[4], p1[4];  // fragment rows gq and gq + 8
@@ -222,7 +232,7 @@ __device__ __forceinline__ void consume_chunk(const unsigned char* wsl, uint32_t
           }
       }
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -232,19 +242,21 @@ __device__ __forceinline__ void consume_chunk(const unsigned char* wsl, uint32_t
 #pragma unroll
     for (int ss = 0; ss < NST; ++ss) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) fp4_row_multipliers<FMT>(wsl + PF::stage_off(ss), F.rows[i][h], m[i][h]);
-      const unsigned char* codes = wsl + PF::codes_off(ss);
-      uint2 wv[2][2];
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t a = wsl + PF::stage_off(ss) + F.sc_off[i][h];
+          fp4_row_multipliers<FMT>(FMT == MOE_W_MXFP4 ? lds16(a) : lds32(a), m[i][h]);
+        }
+      uint2 wv[kSmallMI][2];
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) wv[i][h] = *reinterpret_cast<const uint2*>(codes + F.code_off[i][h]);
+        for (int h = 0; h < 2; ++h) wv[i][h] = lds64(wsl + PF::codes_off(ss) + F.code_off[i][h]);
       uint32_t bf[4][NT][2];
       load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t p0[4], p1[4];
@@ -331,34 +343,44 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     const int cw = warp - 1;
     const int gq = lane >> 2, tq = lane & 3;
     SmallFrag<NT> F;
-    int (&rows)[2][2] = F.rows;
+    int (&rows)[kSmallMI][2] = F.rows;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSmallMI; ++i) {
       if (GATED) {  // gate feature f in fragment row gq, its up row in gq + 8
-        rows[i][0] = 16 * cw + 8 * i + gq;
+        rows[i][0] = 8 * (kSmallMI * cw + i) + gq;
         rows[i][1] = 128 + rows[i][0];
       } else {
-        rows[i][0] = 32 * cw + 16 * i + gq;
+        rows[i][0] = 16 * (kSmallMI * cw + i) + gq;
         rows[i][1] = rows[i][0] + 8;
       }
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) F.code_off[i][h] = (uint32_t)(((tq >> 1) * 256 + rows[i][h]) * 16 + (tq & 1) * 8);
+      for (int h = 0; h < 2; ++h) {
+        F.code_off[i][h] = (uint32_t)(((tq >> 1) * 256 + rows[i][h]) * 16 + (tq & 1) * 8);
+        F.sc_off[i][h] = (uint32_t)(rows[i][h] * (FMT == MOE_W_NVFP4 ? 4 : 2));
+      }
+    // ldmatrix row addresses: token row n, 16-byte chunk c of a stage block sits
+    // at n * 128 + ((c ^ (n & 7)) << 4) (the TMA's 128-byte swizzle)
     if (NT == 1) {
-      F.b_row[0] = (uint32_t)(lane & 7);
-      F.b_sel = (uint32_t)(lane >> 3);  // chunk offset 0..3 (two K-steps per load)
-    } else {
+      const uint32_t n = (uint32_t)(lane & 7), sel = (uint32_t)(lane >> 3);  // two K-steps per load
 #pragma unroll
-      for (int q = 0; q < (NT > 1 ? NT / 2 : 1); ++q) F.b_row[q] = (uint32_t)(16 * q + (lane & 7) + 8 * (lane >> 4));
-      F.b_sel = (uint32_t)((lane >> 3) & 1);
+      for (int j = 0; j < 4; ++j) F.b_off[j][0] = n * 128 + ((((uint32_t)(2 * (j & ~1)) + sel) ^ (n & 7)) << 4);
+    } else {
+      const uint32_t sel = (uint32_t)((lane >> 3) & 1);
+#pragma unroll
+      for (int q = 0; q < SmallFrag<NT>::NQ; ++q) {
+        const uint32_t n = (uint32_t)(16 * q + (lane & 7) + 8 * (lane >> 4));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) F.b_off[j][q] = n * 128 + ((((uint32_t)(2 * j) + sel) ^ (n & 7)) << 4);
+      }
     }
     const float* gs_tab = reinterpret_cast<const float*>(g.packed + (GATED ? L.gs13_off : L.gs2_off));
     const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (GATED ? L.b13_off : L.b2_off));
     const int Npad = L.Npad;
     const int width = GATED ? 2 * Npad : L.K;
-    uint32_t m[2][2][4] = {};
+    uint32_t m[kSmallMI][2][4] = {};
     uint32_t ck = 0;
 
     for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
@@ -366,9 +388,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       decode_item(plan, w, b, tile, split);
       stage_range(plan, L, split, s0, s1);
       const int e = g.expert_ids[b];
-      float acc[2][NT][4];
+      float acc[kSmallMI][NT][4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -377,8 +399,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
         const int slot = ck % kSlots;
         mbar_wait(&full[slot], (ck / kSlots) & 1, abort_flag, g.status);
-        const unsigned char* wsl = smem + slot * SM::kSlotBytes;
-        const uint32_t bsl = smem_u32(wsl + kSmallWBytes);
+        const uint32_t wsl = smem_u32(smem + slot * SM::kSlotBytes);
+        const uint32_t bsl = wsl + kSmallWBytes;
         const int nst = min(kSmallChunk, s1 - c0);
         if (nst == 4) consume_chunk<FMT, NT, BN, 4>(wsl, bsl, F, acc, m);
         else if (nst == 2) consume_chunk<FMT, NT, BN, 2>(wsl, bsl, F, acc, m);
@@ -394,7 +416,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       if (plan.S > 1) {
         // store this slice's fp32 partial, rows by sorted position
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
           for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -402,7 +424,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
               const int pos = b * g.block_m + n * 8 + 2 * tq + c;
               float* dst = g.partial + ((int64_t)split * g.split_rows + pos) * width;
               if (GATED) {
-                const int f = tile * 128 + 16 * cw + 8 * i + gq;
+                const int f = tile * 128 + rows[i][0];
                 __stcg(dst + f, acc[i][n][c]);
                 __stcg(dst + Npad + f, acc[i][n][2 + c]);
               } else {
@@ -427,14 +449,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         __threadfence();
         // sum all slices in split order
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
           for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
         for (int sp = 0; sp < plan.S; ++sp)
 #pragma unroll
-          for (int i = 0; i < 2; ++i)
+          for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -442,7 +464,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
                 const int pos = b * g.block_m + n * 8 + 2 * tq + c;
                 const float* src = g.partial + ((int64_t)sp * g.split_rows + pos) * width;
                 if (GATED) {
-                  const int f = tile * 128 + 16 * cw + 8 * i + gq;
+                  const int f = tile * 128 + rows[i][0];
                   acc[i][n][c] += __ldcg(src + f);
                   acc[i][n][2 + c] += __ldcg(src + Npad + f);
                 } else {
@@ -456,9 +478,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       }
       const float gsc = gs_tab[e];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kSmallMI; ++i) {
         if (GATED) {
-          const int f = tile * 128 + 16 * cw + 8 * i + gq;
+          const int f = tile * 128 + rows[i][0];
           float bg = 0.f, bu = 0.f;
           if (g.has_bias) {
             bg = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + f]);
