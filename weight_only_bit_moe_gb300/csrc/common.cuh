@@ -98,15 +98,26 @@ __host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
   return true;
 }
 
-// Byte offset of stage s inside a tile, whether it carries scales, and its size.
+// Byte offset of stage s inside a tile and whether it carries scales.
 __host__ __device__ inline int64_t stage_offset(const Layout& L, int s) {
   const int q = s / L.period, r = s % L.period;
   return q * L.period_bytes + (r == 0 ? 0 : L.scale_bytes + (int64_t)r * kPackedStageBytes);
 }
 __host__ __device__ inline bool stage_has_scales(const Layout& L, int s) { return s % L.period == 0; }
-__host__ __device__ inline int stage_bytes(const Layout& L, int s) {
-  return kPackedStageBytes + (stage_has_scales(L, s) ? L.scale_bytes : 0);
-}
+
+// Compile-time view of one format's packed stages (the Layout fields period,
+// scale_bytes and period_bytes as constants): stage ss of a chunk that starts
+// on a scale period begins at stage_off(ss); its codes at codes_off(ss).
+template <int FMT>
+struct PackedFmt {
+  static constexpr int kPeriod = FMT == MOE_W_INT4_U4B8 ? 2 : 1;
+  static constexpr int kScaleBytes = kTileRows * (FMT == MOE_W_NVFP4 ? 4 : 2);
+  static constexpr int kPeriodBytes = kScaleBytes + kPeriod * kPackedStageBytes;
+  __host__ __device__ static constexpr int stage_off(int ss) {
+    return (ss / kPeriod) * kPeriodBytes + (ss % kPeriod ? kScaleBytes + (ss % kPeriod) * kPackedStageBytes : 0);
+  }
+  __host__ __device__ static constexpr int codes_off(int ss) { return (ss / kPeriod) * kPeriodBytes + kScaleBytes + (ss % kPeriod) * kPackedStageBytes; }
+};
 
 // Epilogue factor applied to fp32 accumulators.  FP4 formats dequantise to
 // value * 2^-8 (see dequant below), NVFP4 also carries its global scale.
@@ -209,6 +220,29 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Shared-memory loads through 32-bit shared addresses (ordered after the
+// barrier waits like every other volatile access).
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return v;
 }
 
 // Order this thread's generic-proxy shared-memory writes before later

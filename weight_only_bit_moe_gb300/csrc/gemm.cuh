@@ -87,7 +87,7 @@ struct GemmSmem {
   static constexpr int kBar = kP + kSP * kPackedSlotBytes;
   // barriers: p_full, p_empty, a_full, a_empty, b_full, b_empty, acc_full, acc_empty, drain
   static constexpr int kNumBars = 2 * kSP + 2 * kSA + 2 * kSB + 2 * kNacc + 1;
-  static constexpr int kEpiSid = kBar + kNumBars * 8;  // epilogue copy of the block's sorted ids
+  static constexpr int kEpiSid = (kBar + kNumBars * 8 + 15) / 16 * 16;  // epilogue copy of the block's sorted ids
   static constexpr int kMisc = kEpiSid + BN * 4;
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -168,6 +168,7 @@ __device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap* map,
 template <int FMT, bool GATED, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
   using SM = GemmSmem<BN>;
+  using PF = PackedFmt<FMT>;
   constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   uint64_t* acc_empty = acc_full + kNacc;
   uint64_t* drain_bar = acc_empty + kNacc;
   int32_t* epi_sid = reinterpret_cast<int32_t*>(smem + SM::kEpiSid);
+  const uint32_t epi_sid_s = smem_u32(epi_sid);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + SM::kMisc);  // [0] tmem base, [1] abort, [2] last flag
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[1]);
 
@@ -228,9 +230,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         for (int s = s0; s < s1; ++s, ++pk, ++bk) {
           const int slot = pk % kSP;
           mbar_wait(&p_empty[slot], ((pk / kSP) + 1) & 1, abort_flag, g.status);
-          const int bytes = stage_bytes(L, s);
+          const int r = s % PF::kPeriod;  // stage within its scale period; r == 0 carries the scales
+          const int bytes = kPackedStageBytes + (r == 0 ? PF::kScaleBytes : 0);
+          const int64_t off = (int64_t)(s / PF::kPeriod) * PF::kPeriodBytes +
+                              (r == 0 ? 0 : PF::kScaleBytes + r * kPackedStageBytes);
           mbar_arrive_expect_tx(&p_full[slot], bytes);
-          bulk_g2s(smem + SM::kP + slot * kPackedSlotBytes, tb + stage_offset(L, s), bytes, &p_full[slot], pol);
+          bulk_g2s(smem + SM::kP + slot * kPackedSlotBytes, tb + off, bytes, &p_full[slot], pol);
           const int bs = bk % kSB;
           mbar_wait(&b_empty[bs], ((bk / kSB) + 1) & 1, abort_flag, g.status);
           mbar_arrive_expect_tx(&b_full[bs], kBBytes);
@@ -270,10 +275,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           mbar_wait(&a_full[as], (ak / kSA) & 1, abort_flag, g.status);
           mbar_wait(&b_full[bs], (bk / kSB) & 1, abort_flag, g.status);
           tc_fence_after();
-          const uint32_t a_t = tmem_base + as * kAColsPerStage, bbase = b0 + bs * kBBytes;
+          const uint32_t a_t = tmem_base + as * kAColsPerStage;
+          const uint64_t bd0 = smem_desc_sw128(b0 + bs * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kStageK / 16; ++kk) {
-            const uint64_t bd = smem_desc_sw128(bbase + kk * 32);
+            const uint64_t bd = bd0 + (uint64_t)(2 * kk);  // start address advances 32 bytes per K=16 step
             const uint32_t acc = (s > s0 || kk > 0) ? 1u : 0u;
             umma_f16_tmem_a(d0, a_t + kk * 8, bd, idesc, acc);
             umma_f16_tmem_a(d0 + BN, a_t + 32 + kk * 8, bd, idesc, acc);
@@ -306,21 +312,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       for (int s = s0; s < s1; ++s, ++pk, ++ak) {
         const int ps = pk % kSP, as = ak % kSA;
         mbar_wait(&p_full[ps], (pk / kSP) & 1, abort_flag, g.status);
-        const unsigned char* slot = smem + SM::kP + ps * kPackedSlotBytes;
-        const bool has_sc = stage_has_scales(L, s);
+        const uint32_t slot = smem_u32(smem + SM::kP) + (uint32_t)ps * kPackedSlotBytes;
+        const bool has_sc = (s % PF::kPeriod) == 0;
         if (has_sc) {
           if (FMT == MOE_W_INT4_U4B8) {
-            const uint32_t h = bf16_scale_f16(reinterpret_cast<const uint16_t*>(slot)[r]);
+            const uint32_t h = bf16_scale_f16(lds16(slot + 2 * r));
             const uint32_t h16 = __half_as_ushort(__hmul(__ushort_as_half((uint16_t)h), __ushort_as_half(0x2C00)));
             m[0] = h | (h << 16);      // s
             m[1] = h16 | (h16 << 16);  // s / 16
           } else if (FMT == MOE_W_MXFP4) {
-            const uint32_t sv = reinterpret_cast<const uint16_t*>(slot)[r];
+            const uint32_t sv = lds16(slot + 2 * r);
             const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
             m[0] = a | (a << 16);
             m[1] = c | (c << 16);
           } else {
-            const uint32_t sv = reinterpret_cast<const uint32_t*>(slot)[r];
+            const uint32_t sv = lds32(slot + 4 * r);
             const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
             m[0] = __byte_perm(lo, 0, 0x1010);
             m[1] = __byte_perm(lo, 0, 0x3232);
@@ -328,8 +334,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             m[3] = __byte_perm(hi, 0, 0x3232);
           }
         }
-        const uint4* units = reinterpret_cast<const uint4*>(slot + (has_sc ? L.scale_bytes : 0));
-        const uint4 u0 = units[r], u1 = units[256 + r];
+        const uint32_t units = slot + (has_sc ? PF::kScaleBytes : 0) + 16 * r;
+        const uint4 u0 = lds128(units), u1 = lds128(units + 256 * 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[ps]);
         const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -428,48 +434,71 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         if (finish) __threadfence();
       }
       if (finish) {
-        for (int c0 = 8 * csub; c0 < BN; c0 += 16) {
+        // This thread's token columns come in batches of 8: c0 = 8 * csub + 16 * it.
+        // Each batch loads its 8 sorted ids at once, computes all 8 values and then
+        // stores them, so the columns overlap; the next batch's accumulators are
+        // requested from TMEM before this batch's math.
+        constexpr int kIters = BN / 16;
+        uint32_t v0[8], v1[8];
+        if (plan.S == 1) {
+          tmem_ld8(tb + 8 * csub, v0);
+          tmem_ld8(tb + BN + 8 * csub, v1);
+        }
+#pragma unroll 1
+        for (int it = 0; it < kIters; ++it) {
+          const int c0 = 8 * csub + 16 * it;
           float f0[8], f1[8];
           if (plan.S == 1) {
-            uint32_t v0[8], v1[8];
-            tmem_ld8(tb + c0, v0);
-            tmem_ld8(tb + BN + c0, v1);
             tmem_ld_wait();
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) { f0[jj] = __uint_as_float(v0[jj]); f1[jj] = __uint_as_float(v1[jj]); }
+            if (it + 1 < kIters) {
+              tmem_ld8(tb + c0 + 16, v0);
+              tmem_ld8(tb + BN + c0 + 16, v1);
+            } else {  // every accumulator column of this thread is in registers
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[accb]);
+            }
           } else {
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) { f0[jj] = 0.f; f1[jj] = 0.f; }
             for (int sp = 0; sp < plan.S; ++sp)
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) {
-                if (c0 + jj >= jmax) break;
-                const float* src = g.partial + ((int64_t)sp * g.split_rows + b * g.block_m + c0 + jj) * width;
-                if (ok0) f0[jj] += __ldcg(src + col0);
-                if (ok1) f1[jj] += __ldcg(src + col1);
+                if (c0 + jj < jmax) {
+                  const float* src = g.partial + ((int64_t)sp * g.split_rows + b * g.block_m + c0 + jj) * width;
+                  if (ok0) f0[jj] += __ldcg(src + col0);
+                  if (ok1) f1[jj] += __ldcg(src + col1);
+                }
               }
           }
+          const uint4 sa = lds128(epi_sid_s + 4 * c0), sb = lds128(epi_sid_s + 4 * c0 + 16);
+          const int sid[8] = {(int)sa.x, (int)sa.y, (int)sa.z, (int)sa.w, (int)sb.x, (int)sb.y, (int)sb.z, (int)sb.w};
+          const int pos0 = b * g.block_m + c0;
+          if (GATED) {
+            float av[8];
+            if (g.act_kind == MOE_ACT_SILU_MUL) {
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            if (c0 + jj >= jmax) break;
-            const int pos = b * g.block_m + c0 + jj;
-            const int sid = epi_sid[c0 + jj];
-            if (GATED) {
-              const float hg = f0[jj] * gsc + bias0;
-              const float hu = f1[jj] * gsc + bias1;
-              const float a = sid < g.pairs ? act_fn(g.act_kind, hg, hu, g.alpha, g.limit) : 0.0f;
-              g.a_out[(int64_t)pos * Npad + row0] = __half_as_ushort(__float2half_rn(a));
-            } else if (sid < g.pairs) {
-              float* dst = g.y_out + (int64_t)sid * L.K;
-              if (ok0) dst[row0] = f0[jj] * gsc + bias0;
-              if (ok1) dst[row1] = f1[jj] * gsc + bias1;
+              for (int jj = 0; jj < 8; ++jj) av[jj] = act_fn(MOE_ACT_SILU_MUL, f0[jj] * gsc + bias0, f1[jj] * gsc + bias1, 0.f, 0.f);
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj)
+                av[jj] = act_fn(MOE_ACT_SIGMOID_ALPHA, f0[jj] * gsc + bias0, f1[jj] * gsc + bias1, g.alpha, g.limit);
             }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+              if (c0 + jj < jmax)
+                g.a_out[(int64_t)(pos0 + jj) * Npad + row0] = __half_as_ushort(__float2half_rn(sid[jj] < g.pairs ? av[jj] : 0.0f));
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+              if (c0 + jj < jmax && sid[jj] < g.pairs) {
+                float* dst = g.y_out + (int64_t)sid[jj] * L.K;
+                if (ok0) dst[row0] = f0[jj] * gsc + bias0;
+                if (ok1) dst[row1] = f1[jj] * gsc + bias1;
+              }
           }
-        }
-        if (plan.S == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[accb]);
         }
       }
     }

@@ -91,20 +91,6 @@ __device__ __forceinline__ void tma_tile3d(uint32_t dst, const CUtensorMap* map,
       : "memory");
 }
 
-// Compile-time view of one format's packed stages (the Layout fields period,
-// scale_bytes and period_bytes as constants): stage ss of a chunk that starts
-// on a scale period begins at stage_off(ss); its codes at codes_off(ss).
-template <int FMT>
-struct PackedFmt {
-  static constexpr int kPeriod = FMT == MOE_W_INT4_U4B8 ? 2 : 1;
-  static constexpr int kScaleBytes = kTileRows * (FMT == MOE_W_NVFP4 ? 4 : 2);
-  static constexpr int kPeriodBytes = kScaleBytes + kPeriod * kPackedStageBytes;
-  __host__ __device__ static constexpr int stage_off(int ss) {
-    return (ss / kPeriod) * kPeriodBytes + (ss % kPeriod ? kScaleBytes + (ss % kPeriod) * kPackedStageBytes : 0);
-  }
-  __host__ __device__ static constexpr int codes_off(int ss) { return (ss / kPeriod) * kPeriodBytes + kScaleBytes + (ss % kPeriod) * kPackedStageBytes; }
-};
-
 // 8 INT4 (uint4b8) codes of one word -> its 4 pairs of (q - 8) as f16x2, exact:
 // pairs 0 and 2 are (1024 + q) - 1032, pairs 1 and 3 (1024 + 16q) / 16 - 72.
 __device__ __forceinline__ void int4x8_f16_unscaled(uint32_t w, uint32_t (&o)[4]) {
@@ -120,24 +106,6 @@ __device__ __forceinline__ void int4x8_f16_unscaled(uint32_t w, uint32_t (&o)[4]
     const __half2 r = (i & 1) ? __hfma2(x, r16, cm72) : __hsub2(x, c1032);
     o[i] = *reinterpret_cast<const uint32_t*>(&r);
   }
-}
-
-// Shared-memory loads through 32-bit shared addresses (ordered after the
-// barrier waits like every other volatile access).
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t lds16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-  return v;
 }
 
 // f16x2 multipliers of one FP4 row from its scale bytes: MXFP4 one per 32 K
@@ -322,8 +290,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
           const int c1 = min(c0 + kSmallChunk, s1);
           const int slot = ck % kSlots;
           mbar_wait(&empty[slot], ((ck / kSlots) + 1) & 1, abort_flag, g.status);
-          const int64_t off0 = stage_offset(L, c0);
-          const uint32_t wbytes = (uint32_t)(stage_offset(L, c1) - off0);
+          // c0 and c1 lie on scale-period boundaries
+          const int64_t off0 = (int64_t)(c0 / PackedFmt<FMT>::kPeriod) * PackedFmt<FMT>::kPeriodBytes;
+          const uint32_t wbytes = (uint32_t)((c1 - c0) / PackedFmt<FMT>::kPeriod * PackedFmt<FMT>::kPeriodBytes);
           unsigned char* dst = smem + slot * SM::kSlotBytes;
           mbar_arrive_expect_tx(&full[slot], wbytes + SM::kBBytes);
           bulk_g2s(dst, tb + off0, wbytes, &full[slot], pol);
