@@ -258,43 +258,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(128, BN, 0u);
-      uint32_t ak = 0, bk = 0, ic = 0;
-      const uint32_t b0 = smem_u32(smem + SM::kB);
-      for (int w = blockIdx.x; w < plan.items; w += gridDim.x, ++ic) {
-        int b, tile, split, s0, s1;
-        decode_item(plan, w, b, tile, split);
-        stage_range(plan, L, split, s0, s1);
-        const int accb = ic % kNacc;
-        mbar_wait(&acc_empty[accb], ((ic / kNacc) + 1) & 1, abort_flag, g.status);
+    // The whole warp runs the loop so descriptors and TMEM addresses are
+    // warp-uniform; one elected lane issues.  __syncwarp reconverges the warp
+    // after each wait before the elected issue.
+    constexpr uint32_t idesc = idesc_f16_f32(128, BN, 0u);
+    uint32_t ak = 0, bk = 0, ic = 0;
+    const uint32_t b0 = smem_u32(smem + SM::kB);
+    for (int w = blockIdx.x; w < plan.items; w += gridDim.x, ++ic) {
+      int b, tile, split, s0, s1;
+      decode_item(plan, w, b, tile, split);
+      stage_range(plan, L, split, s0, s1);
+      const int accb = ic % kNacc;
+      mbar_wait(&acc_empty[accb], ((ic / kNacc) + 1) & 1, abort_flag, g.status);
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t d0 = tmem_base + kAccCol0 + accb * 2 * BN;
+      for (int s = s0; s < s1; ++s, ++ak, ++bk) {
+        const int as = ak % kSA, bs = bk % kSB;
+        mbar_wait(&a_full[as], (ak / kSA) & 1, abort_flag, g.status);
+        mbar_wait(&b_full[bs], (bk / kSB) & 1, abort_flag, g.status);
+        __syncwarp();
         tc_fence_after();
-        const uint32_t d0 = tmem_base + kAccCol0 + accb * 2 * BN;
-        for (int s = s0; s < s1; ++s, ++ak, ++bk) {
-          const int as = ak % kSA, bs = bk % kSB;
-          mbar_wait(&a_full[as], (ak / kSA) & 1, abort_flag, g.status);
-          mbar_wait(&b_full[bs], (bk / kSB) & 1, abort_flag, g.status);
-          tc_fence_after();
-          const uint32_t a_t = tmem_base + as * kAColsPerStage;
-          const uint64_t bd0 = smem_desc_sw128(b0 + bs * kBBytes);
+        const uint32_t a_t = tmem_base + as * kAColsPerStage;
+        const uint64_t bd0 = smem_desc_sw128(b0 + bs * kBBytes);
 #pragma unroll
-          for (int kk = 0; kk < kStageK / 16; ++kk) {
-            const uint64_t bd = bd0 + (uint64_t)(2 * kk);  // start address advances 32 bytes per K=16 step
-            const uint32_t acc = (s > s0 || kk > 0) ? 1u : 0u;
-            umma_f16_tmem_a(d0, a_t + kk * 8, bd, idesc, acc);
-            umma_f16_tmem_a(d0 + BN, a_t + 32 + kk * 8, bd, idesc, acc);
-          }
-          umma_commit(&a_empty[as]);
-          umma_commit(&b_empty[bs]);
+        for (int kk = 0; kk < kStageK / 16; ++kk) {
+          const uint64_t bd = bd0 + (uint64_t)(2 * kk);  // start address advances 32 bytes per K=16 step
+          const uint32_t acc = (s > s0 || kk > 0) ? 1u : 0u;
+          umma_f16_tmem_a_elect(d0, a_t + kk * 8, bd, idesc, acc);
+          umma_f16_tmem_a_elect(d0 + BN, a_t + 32 + kk * 8, bd, idesc, acc);
         }
-        umma_commit(&acc_full[accb]);
+        umma_commit_elect(&a_empty[as]);
+        umma_commit_elect(&b_empty[bs]);
       }
-      // all issued MMAs complete before TMEM is released
-      umma_commit(drain_bar);
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < 100000000ull) {
-      }
+      umma_commit_elect(&acc_full[accb]);
     }
+    // all issued MMAs complete before TMEM is released
+    umma_commit_elect(drain_bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < 100000000ull) {
+    }
+    __syncwarp();
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant warps
     // warp -> (TMEM lane quarter q = warp % 4, half): a warp may only touch TMEM
