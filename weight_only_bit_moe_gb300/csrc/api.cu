@@ -106,21 +106,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Row-major [rows, cols] 16-bit matrix, 128-byte swizzled boxes of box_rows x 64.
-bool make_act_map(CUtensorMap* m, const void* base, bool f16, int64_t cols, int64_t rows, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-  const cuuint32_t es[2] = {1u, 1u};
-  return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The same matrix viewed as [rows][cols / 64][64]: dims (64, rows, cols / 64),
+// A row-major [rows, cols] fp16 matrix viewed as [rows][cols / 64][64]: dims (64, rows, cols / 64),
 // boxes of 64 x box_rows x box_stages landing as [stage][row][64] with the
 // 128-byte swizzle, so one copy brings several 64-column stages.
 bool make_act_map3(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int box_rows, int box_stages) {
@@ -201,13 +187,9 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   GemmArgs g{};
   // GEMM1 reads the gathered fp16 rows; GEMM2 GEMM1's fp16 output
   CUtensorMap map2;
-  if (small) {
-    if (!make_act_map3(&g.tmap_b, ws + w.xs_off, L.K, w.cap, bn, kSmallChunk)) return MOE_ERR_CUDA;
-    if (!make_act_map3(&map2, ws + w.a_off, L.Npad, w.cap, bn, kSmallChunk)) return MOE_ERR_CUDA;
-  } else {
-    if (!make_act_map(&g.tmap_b, ws + w.xs_off, true, L.K, w.cap, bn)) return MOE_ERR_CUDA;
-    if (!make_act_map(&map2, ws + w.a_off, true, L.Npad, w.cap, bn)) return MOE_ERR_CUDA;
-  }
+  const int box_stages = small ? kSmallChunk : kSup;  // 64-K stages per activation copy
+  if (!make_act_map3(&g.tmap_b, ws + w.xs_off, L.K, w.cap, bn, box_stages)) return MOE_ERR_CUDA;
+  if (!make_act_map3(&map2, ws + w.a_off, L.Npad, w.cap, bn, box_stages)) return MOE_ERR_CUDA;
 
   // prologue: status word and split-K counters to zero, routed rows gathered
   PrepArgs pa{};

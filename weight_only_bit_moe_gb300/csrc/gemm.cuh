@@ -20,18 +20,18 @@
 //   * operands are fp16 x fp16: every dequantised weight is exact in fp16, and
 //     the activation operand keeps 11 significant bits.  Accumulation, bias,
 //     scales and the activation are fp32;
-//   * one producer thread keeps both streams in flight with TMA: a 1-D bulk
-//     copy of each stage's packed codes + scales (one contiguous chunk thanks to
-//     the repack) and a 2-D tile of the block's activation rows (GEMM1: the rows
-//     the prologue gathered in sorted order; GEMM2: GEMM1's output), landing in
-//     the 128-byte swizzled K-major layout;
+//   * two producer threads, one per operand stream, keep both in flight with
+//     TMA: a 1-D bulk copy of each stage's packed codes + scales (one
+//     contiguous chunk thanks to the repack) and a 2-D tile of the block's
+//     activation rows (GEMM1: the rows the prologue gathered in sorted order;
+//     GEMM2: GEMM1's output), landing in the 128-byte swizzled K-major layout;
 //   * a persistent grid (one CTA per SM) walks work items (tile, K-split, block)
 //     with the tile index fastest, so the tiles of one block run together and
 //     its activation rows are read from L2; K is split on the device when there
 //     are too few items to fill the GPU (decode), and the last CTA to arrive on
 //     an item's counter sums the fp32 partials in split order (bitwise
 //     reproducible, no spinning);
-//   * one thread issues tcgen05.mma into TMEM accumulators (double-buffered up
+//   * one elected lane of the MMA warp issues tcgen05.mma into TMEM accumulators (double-buffered up
 //     to 64 tokens); eight epilogue warps (two per TMEM lane quarter, splitting
 //     the token columns) add bias and scales, apply the activation (GEMM1) or
 //     write rows to their pairs (GEMM2).
@@ -43,20 +43,22 @@
 
 namespace moe {
 
-constexpr int kSA = 4;                 // dequantised-A ring (in TMEM)
+constexpr int kSup = 2;                // 64-K stages per pipeline unit (one barrier round per unit)
+constexpr int kSA = 2;                 // dequantised-A ring in TMEM, in units
 constexpr int kNumDequantWarps = 8;
 constexpr int kNumEpiWarps = 8;                             // two per TMEM lane quarter
 constexpr int kEpiThreads = kNumEpiWarps * 32;
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpDequant0 = 2;
-constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 10..17
-constexpr int kGemmThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 576
-constexpr int kPackedSlotBytes = kPackedStageBytes + 1024;  // codes + largest scale block
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpBProducer = 2, kWarpDequant0 = 3;
+constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..18
+constexpr int kGemmThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 608
+constexpr int kPackedSlotBytes = kSup * (kPackedStageBytes + 1024);  // a unit's codes + largest scale blocks
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint32_t kTmemCols = 512;                         // whole TMEM (one CTA per SM)
 constexpr uint32_t kAColsPerStage = 64;                     // 2 halves x 64 K / 2 per column
+constexpr uint32_t kAColsPerUnit = kSup * kAColsPerStage;
 
 struct GemmArgs {
-  CUtensorMap tmap_b;         // activation rows [rows, Kred] 16-bit, 64 x BN boxes
+  CUtensorMap tmap_b;         // activation rows [rows, Kred] 16-bit as 3-D boxes of 64 x BN x stages
   Layout L;
   const uint8_t* packed;      // repacked blob
   const int32_t* sorted_ids;
@@ -79,11 +81,12 @@ struct GemmArgs {
 template <int BN>
 struct GemmSmem {
   static constexpr int kNacc = BN >= 128 ? 1 : 2;                                   // TMEM accumulators
-  static constexpr int kSB = BN <= 16 ? 16 : (BN <= 32 ? 12 : (BN <= 64 ? 8 : 6));  // activation ring
+  static constexpr int kBUnitBytes = kSup * BN * 128;  // activation rows of a unit, [stage][row][64]
+  static constexpr int kSB = BN <= 64 ? 6 : 4;           // activation ring, in units
   static constexpr int kB = 0;
-  static constexpr int kP = kB + kSB * BN * 128;
+  static constexpr int kP = kB + kSB * kBUnitBytes;
   static constexpr int kSPfit = (kSmemBudget - kP - 3072) / kPackedSlotBytes;
-  static constexpr int kSP = kSPfit > 16 ? 16 : kSPfit;  // packed-weight ring
+  static constexpr int kSP = kSPfit > 8 ? 8 : kSPfit;  // packed-weight ring, in units
   static constexpr int kBar = kP + kSP * kPackedSlotBytes;
   // barriers: p_full, p_empty, a_full, a_empty, b_full, b_empty, acc_full, acc_empty, drain
   static constexpr int kNumBars = 2 * kSP + 2 * kSA + 2 * kSB + 2 * kNacc + 1;
@@ -91,9 +94,9 @@ struct GemmSmem {
   static constexpr int kMisc = kEpiSid + BN * 4;
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
-  static_assert(kSP >= 8, "packed ring too shallow");
+  static_assert(kSP >= 4, "packed ring too shallow");
   static_assert(kAlloc <= 232448, "shared memory over the per-CTA limit");
-  static_assert(kSA * kAColsPerStage + kNacc * 2 * BN <= kTmemCols, "TMEM over budget");
+  static_assert(kSA * kAColsPerUnit + kNacc * 2 * BN <= kTmemCols, "TMEM over budget");
 };
 
 // Gated activations in fp32 with the fast exponential and division intrinsics
@@ -156,12 +159,13 @@ __device__ __forceinline__ void stage_range(const WorkPlan& p, const Layout& L, 
   s1 = (split + 1) * p.units / p.S * L.period;
 }
 
-// TMA: a 2-D tile (box from the tensor map) at (col, row).
-__device__ __forceinline__ void tma_tile2d(uint32_t dst, const CUtensorMap* map, int col, int row, uint64_t* bar) {
+// TMA: a 3-D tile (box from the tensor map) at (c0, c1, c2).
+__device__ __forceinline__ void tma_tile3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                           uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(row), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Layout& L = g.L;
   constexpr uint32_t kBBytes = BN * 128;                      // activation bytes per stage
-  constexpr uint32_t kAccCol0 = kSA * kAColsPerStage;        // accumulators after the A ring
+  constexpr uint32_t kAccCol0 = kSA * kAColsPerUnit;         // accumulators after the A ring
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], kNumDequantWarps); }
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     tmem_alloc(&misc[0], kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpProducer && lane == 0)
+  if (warp == kWarpBProducer && lane == 0)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g.tmap_b)) : "memory");
   tc_fence_before();
   __syncthreads();
@@ -217,29 +221,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   const uint8_t* wbase = g.packed + (GATED ? L.w13_off : L.w2_off);
 
   if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ TMA producer (weights + activation rows)
+    // ------------------------------------------------------------ TMA producer (packed weights)
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      uint32_t pk = 0, bk = 0;
+      uint32_t pk = 0;
       for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
         int b, tile, split, s0, s1;
         decode_item(plan, w, b, tile, split);
         stage_range(plan, L, split, s0, s1);
         const int e = g.expert_ids[b];
         const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
-        for (int s = s0; s < s1; ++s, ++pk, ++bk) {
+        for (int s = s0; s < s1; s += kSup, ++pk) {
           const int slot = pk % kSP;
           mbar_wait(&p_empty[slot], ((pk / kSP) + 1) & 1, abort_flag, g.status);
-          const int r = s % PF::kPeriod;  // stage within its scale period; r == 0 carries the scales
-          const int bytes = kPackedStageBytes + (r == 0 ? PF::kScaleBytes : 0);
-          const int64_t off = (int64_t)(s / PF::kPeriod) * PF::kPeriodBytes +
-                              (r == 0 ? 0 : PF::kScaleBytes + r * kPackedStageBytes);
+          // a unit starts on a scale period and holds whole periods (INT4 ranges are even)
+          const int nst = min(kSup, s1 - s);
+          const int bytes = nst / PF::kPeriod * PF::kPeriodBytes;
+          const int64_t off = (int64_t)(s / PF::kPeriod) * PF::kPeriodBytes;
           mbar_arrive_expect_tx(&p_full[slot], bytes);
           bulk_g2s(smem + SM::kP + slot * kPackedSlotBytes, tb + off, bytes, &p_full[slot], pol);
-          const int bs = bk % kSB;
-          mbar_wait(&b_empty[bs], ((bk / kSB) + 1) & 1, abort_flag, g.status);
-          mbar_arrive_expect_tx(&b_full[bs], kBBytes);
-          tma_tile2d(smem_u32(smem + SM::kB + bs * kBBytes), &g.tmap_b, s * kStageK, b * g.block_m, &b_full[bs]);
         }
       }
       // leave no copy in flight: wait for the last phase of every used slot
@@ -247,6 +247,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         const uint32_t k = pk - 1 - i;
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(&p_full[k % kSP], (k / kSP) & 1) && global_timer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else if (warp == kWarpBProducer) {
+    // ------------------------------------------------------------ TMA producer (activation rows)
+    if (lane == 0) {
+      uint32_t bk = 0;
+      for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
+        int b, tile, split, s0, s1;
+        decode_item(plan, w, b, tile, split);
+        stage_range(plan, L, split, s0, s1);
+        for (int s = s0; s < s1; s += kSup, ++bk) {
+          const int bs = bk % kSB;
+          mbar_wait(&b_empty[bs], ((bk / kSB) + 1) & 1, abort_flag, g.status);
+          // one 3-D box brings both stages of the unit (past K it reads zeros)
+          mbar_arrive_expect_tx(&b_full[bs], SM::kBUnitBytes);
+          tma_tile3d(smem_u32(smem + SM::kB + bs * SM::kBUnitBytes), &g.tmap_b, 0, b * g.block_m, s, &b_full[bs]);
         }
       }
       for (uint32_t i = 0; i < (uint32_t)kSB && i < bk; ++i) {
@@ -273,20 +290,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       __syncwarp();
       tc_fence_after();
       const uint32_t d0 = tmem_base + kAccCol0 + accb * 2 * BN;
-      for (int s = s0; s < s1; ++s, ++ak, ++bk) {
+      for (int s = s0; s < s1; s += kSup, ++ak, ++bk) {
         const int as = ak % kSA, bs = bk % kSB;
+        const int nst = min(kSup, s1 - s);
         mbar_wait(&a_full[as], (ak / kSA) & 1, abort_flag, g.status);
         mbar_wait(&b_full[bs], (bk / kSB) & 1, abort_flag, g.status);
         __syncwarp();
         tc_fence_after();
-        const uint32_t a_t = tmem_base + as * kAColsPerStage;
-        const uint64_t bd0 = smem_desc_sw128(b0 + bs * kBBytes);
 #pragma unroll
-        for (int kk = 0; kk < kStageK / 16; ++kk) {
-          const uint64_t bd = bd0 + (uint64_t)(2 * kk);  // start address advances 32 bytes per K=16 step
-          const uint32_t acc = (s > s0 || kk > 0) ? 1u : 0u;
-          umma_f16_tmem_a_elect(d0, a_t + kk * 8, bd, idesc, acc);
-          umma_f16_tmem_a_elect(d0 + BN, a_t + 32 + kk * 8, bd, idesc, acc);
+        for (int j = 0; j < kSup; ++j) {
+          if (j < nst) {
+            const uint32_t a_t = tmem_base + as * kAColsPerUnit + j * kAColsPerStage;
+            const uint64_t bd0 = smem_desc_sw128(b0 + bs * SM::kBUnitBytes + j * kBBytes);
+#pragma unroll
+            for (int kk = 0; kk < kStageK / 16; ++kk) {
+              const uint64_t bd = bd0 + (uint64_t)(2 * kk);  // start address advances 32 bytes per K=16 step
+              const uint32_t acc = (s > s0 || j > 0 || kk > 0) ? 1u : 0u;
+              umma_f16_tmem_a_elect(d0, a_t + kk * 8, bd, idesc, acc);
+              umma_f16_tmem_a_elect(d0 + BN, a_t + 32 + kk * 8, bd, idesc, acc);
+            }
+          }
         }
         umma_commit_elect(&a_empty[as]);
         umma_commit_elect(&b_empty[bs]);
@@ -308,57 +331,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     const int r = half * 128 + hr;  // tile row
     const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + half * 32;
     uint32_t pk = 0, ak = 0;
-    uint32_t m[4] = {0, 0, 0, 0};  // f16x2 multipliers (INT4: s, s/16; MXFP4: per 32; NVFP4: per 16)
     for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
       int b, tile, split, s0, s1;
       decode_item(plan, w, b, tile, split);
       stage_range(plan, L, split, s0, s1);
-      for (int s = s0; s < s1; ++s, ++pk, ++ak) {
+      for (int s = s0; s < s1; s += kSup, ++pk, ++ak) {
         const int ps = pk % kSP, as = ak % kSA;
+        const int nst = min(kSup, s1 - s);
         mbar_wait(&p_full[ps], (pk / kSP) & 1, abort_flag, g.status);
         const uint32_t slot = smem_u32(smem + SM::kP) + (uint32_t)ps * kPackedSlotBytes;
-        const bool has_sc = (s % PF::kPeriod) == 0;
-        if (has_sc) {
-          if (FMT == MOE_W_INT4_U4B8) {
-            const uint32_t h = bf16_scale_f16(lds16(slot + 2 * r));
-            const uint32_t h16 = __half_as_ushort(__hmul(__ushort_as_half((uint16_t)h), __ushort_as_half(0x2C00)));
-            m[0] = h | (h << 16);      // s
-            m[1] = h16 | (h16 << 16);  // s / 16
-          } else if (FMT == MOE_W_MXFP4) {
-            const uint32_t sv = lds16(slot + 2 * r);
-            const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
-            m[0] = a | (a << 16);
-            m[1] = c | (c << 16);
-          } else {
-            const uint32_t sv = lds32(slot + 4 * r);
-            const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
-            m[0] = __byte_perm(lo, 0, 0x1010);
-            m[1] = __byte_perm(lo, 0, 0x3232);
-            m[2] = __byte_perm(hi, 0, 0x1010);
-            m[3] = __byte_perm(hi, 0, 0x3232);
+        // codes (and scales) of both stages into registers, then release the slot
+        uint4 u[kSup][2];
+        uint32_t m[kSup][4];  // f16x2 multipliers (INT4: s, s/16; MXFP4: per 32; NVFP4: per 16)
+#pragma unroll
+        for (int j = 0; j < kSup; ++j) {
+          if (j < nst) {
+            const uint32_t st = slot + PF::stage_off(j);
+            if (FMT == MOE_W_INT4_U4B8) {
+              if (j == 0) {  // one scale per 128 K covers both stages
+                const uint32_t h = bf16_scale_f16(lds16(st + 2 * r));
+                const uint32_t h16 = __half_as_ushort(__hmul(__ushort_as_half((uint16_t)h), __ushort_as_half(0x2C00)));
+                m[0][0] = h | (h << 16);      // s
+                m[0][1] = h16 | (h16 << 16);  // s / 16
+              } else {
+                m[j][0] = m[0][0];
+                m[j][1] = m[0][1];
+              }
+            } else if (FMT == MOE_W_MXFP4) {
+              const uint32_t sv = lds16(st + 2 * r);
+              const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
+              m[j][0] = a | (a << 16);
+              m[j][1] = c | (c << 16);
+            } else {
+              const uint32_t sv = lds32(st + 4 * r);
+              const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
+              m[j][0] = __byte_perm(lo, 0, 0x1010);
+              m[j][1] = __byte_perm(lo, 0, 0x3232);
+              m[j][2] = __byte_perm(hi, 0, 0x1010);
+              m[j][3] = __byte_perm(hi, 0, 0x3232);
+            }
+            const uint32_t units = slot + PF::codes_off(j) + 16 * r;
+            u[j][0] = lds128(units);
+            u[j][1] = lds128(units + 256 * 16);
           }
         }
-        const uint32_t units = slot + (has_sc ? PF::kScaleBytes : 0) + 16 * r;
-        const uint4 u0 = lds128(units), u1 = lds128(units + 256 * 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[ps]);
-        const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t o[32];  // TMEM column c = K pair (2c, 2c+1) of the stage
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
-          // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
-          const int t = v >> 1, h = v & 1;
-          uint32_t t4[4];
-          if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[0], m[1], t4);
-          else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[h], m[h], t4);
-          else e2m1x8_f16(wd[v], m[2 * h], m[2 * h + 1], t4);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
-        }
         mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
         tc_fence_after();
-        tmem_st32(t_lane + as * kAColsPerStage, o);
+#pragma unroll
+        for (int j = 0; j < kSup; ++j) {
+          if (j < nst) {
+            const uint32_t wd[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
+                                    u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
+            uint32_t o[32];  // TMEM column c = K pair (2c, 2c+1) of the stage
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
+              // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
+              const int t = v >> 1, h = v & 1;
+              uint32_t t4[4];
+              if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[j][0], m[j][1], t4);
+              else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[j][h], m[j][h], t4);
+              else e2m1x8_f16(wd[v], m[j][2 * h], m[j][2 * h + 1], t4);
+#pragma unroll
+              for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
+            }
+            tmem_st32(t_lane + as * kAColsPerUnit + j * kAColsPerStage, o);
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

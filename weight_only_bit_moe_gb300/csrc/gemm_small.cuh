@@ -81,16 +81,6 @@ __device__ __forceinline__ WorkPlan make_plan_small(const GemmArgs& g, bool gate
   return p;
 }
 
-// TMA: a 3-D tile (box from the tensor map) at (c0, c1, c2).
-__device__ __forceinline__ void tma_tile3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                           uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // 8 INT4 (uint4b8) codes of one word -> its 4 pairs of (q - 8) as f16x2, exact:
 // pairs 0 and 2 are (1024 + q) - 1032, pairs 1 and 3 (1024 + 16q) / 16 - 72.
 __device__ __forceinline__ void int4x8_f16_unscaled(uint32_t w, uint32_t (&o)[4]) {
