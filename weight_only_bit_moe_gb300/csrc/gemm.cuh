@@ -377,8 +377,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[ps]);
-        mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
-        tc_fence_after();
+        // the first stage is dequantised before the wait for its TMEM slot, so
+        // only the stores trail the MMAs that free it
 #pragma unroll
         for (int j = 0; j < kSup; ++j) {
           if (j < nst) {
@@ -396,6 +396,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               else e2m1x8_f16(wd[v], m[j][2 * h], m[j][2 * h + 1], t4);
 #pragma unroll
               for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
+            }
+            if (j == 0) {
+              mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
+              tc_fence_after();
             }
             tmem_st32(t_lane + as * kAColsPerUnit + j * kAColsPerStage, o);
           }
