@@ -42,22 +42,28 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   int* start = count + E;                   // [E]
   __shared__ int warp_sums[32];
 
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int seg = (pairs + kAlignWarps - 1) / kAlignWarps;
   const int p0 = warp * seg, p1 = min(pairs, p0 + seg);
   const uint32_t lt_mask = (1u << lane) - 1u;
   int* row = tab + warp * E;
 
-  // 1. segment counts; a warp loads up to 32 rounds of ids at once (one round
-  //    trip), then counts them
+  // 1. segment counts; a warp loads up to kAlignBatch rounds of 32 ids at once
+  //    (one round trip), then counts them.  A segment that fits one batch keeps
+  //    its ids in registers for the scatter.
   for (int e = lane; e < E; e += 32) row[e] = 0;
   __syncwarp();
+  const bool one_batch = p1 - p0 <= 32 * kAlignBatch;
+  int keep[kAlignBatch];
   for (int pass = p0; pass < p1; pass += 32 * kAlignBatch) {
     int ev[kAlignBatch];
 #pragma unroll
     for (int i = 0; i < kAlignBatch; ++i) {
       const int p = pass + 32 * i + lane;
       ev[i] = p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1;
+      keep[i] = ev[i];
     }
 #pragma unroll
     for (int i = 0; i < kAlignBatch; ++i) {
@@ -125,7 +131,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
 #pragma unroll
     for (int i = 0; i < kAlignBatch; ++i) {
       const int p = pass + 32 * i + lane;
-      ev[i] = p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1;
+      ev[i] = one_batch ? keep[i] : (p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1);
     }
 #pragma unroll
     for (int i = 0; i < kAlignBatch; ++i) {
@@ -170,7 +176,8 @@ extern "C" int moe_align(const int32_t* topk_ids, int M, int top_k, int expert_b
       return MOE_ERR_CUDA;
     configured[dev] = true;
   }
-  align_kernel<<<1, kAlignThreads, smem, (cudaStream_t)stream>>>(topk_ids, M * top_k, expert_base, num_experts,
-                                                                 block_m, cap, sorted_ids, expert_ids, n_padded);
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const cudaError_t err = launch_dependent(align_kernel, dim3(1), dim3(kAlignThreads), smem, (cudaStream_t)stream,
+                                           topk_ids, M * top_k, expert_base, num_experts, block_m, cap, sorted_ids,
+                                           expert_ids, n_padded);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -12,8 +12,9 @@
 //
 // y is fp32.  Each thread owns 8 consecutive columns (two 16-byte loads per
 // slot, one 16-byte bf16 store) and issues every slot's loads before it sums,
-// in slot order.  The plain combine spreads a token over a 2-D grid of column
-// chunks; the post-norm combine keeps one CTA per token for its row reduction.
+// in slot order.  Plain rows spread a token over a 2-D grid of 128-thread
+// column blocks; post-norm rows take one CTA per token, wide enough to cover
+// the row in one pass (up to 1024 threads), so the row reduction stays in it.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,7 +22,6 @@
 
 namespace moe {
 
-constexpr int kCombineThreads = 128;
 constexpr int kCols = 8;  // columns per thread
 constexpr int kMaxTopK = 16;
 
@@ -60,8 +60,10 @@ __device__ __forceinline__ void store8(uint16_t* out, const float (&v)[8]) {
   *reinterpret_cast<uint4*>(out) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineArgs c) {
-  const int t = blockIdx.x, tid = threadIdx.x;
+// blockIdx.x = token; plain rows: blockIdx.y = column block.
+__global__ void __launch_bounds__(1024) combine_kernel(const __grid_constant__ CombineArgs c) {
+  grid_dependency_wait();
+  const int t = blockIdx.x, tid = threadIdx.x, nthreads = blockDim.x;
   const int k = c.top_k;
   int e[kMaxTopK];
   float w[kMaxTopK];
@@ -80,31 +82,31 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   uint16_t* orow = c.out + (int64_t)t * c.K;
 
   if (!c.post_norm_w) {
-    const int col = (blockIdx.y * kCombineThreads + tid) * kCols;
-    if (col >= c.K) return;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int col = (blockIdx.y * nthreads + tid) * kCols; col < c.K; col += gridDim.y * nthreads * kCols) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j >= k) break;
-      if (e[j] < 0) continue;
-      float y[8];
-      pair_y8(c, t * k + j, col, y);
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (j >= k) break;
+        if (e[j] < 0) continue;
+        float y[8];
+        pair_y8(c, t * k + j, col, y);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += w[j] * y[i];
+        for (int i = 0; i < 8; ++i) acc[i] += w[j] * y[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] *= c.rsf;
+      store8(orow + col, acc);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] *= c.rsf;
-    store8(orow + col, acc);
     return;
   }
 
   // post-expert norm: per-slot sum of squares over the whole row first
-  __shared__ float s_red[kCombineThreads / 32][kMaxTopK];
+  __shared__ float s_red[1024 / 32][kMaxTopK];
   __shared__ float s_inv[kMaxTopK];
   float ss[kMaxTopK];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) ss[j] = 0.f;
-  for (int col = tid * kCols; col < c.K; col += kCombineThreads * kCols) {
+  for (int col = tid * kCols; col < c.K; col += nthreads * kCols) {
     float nw[8];
     norm_w8(c.post_norm_w, col, nw);
 #pragma unroll
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
       }
     }
   }
-  const int lane = tid & 31, warp = tid >> 5;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     float v = ss[j];
@@ -131,11 +133,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   __syncthreads();
   if (tid < kMaxTopK) {
     float v = 0.f;
-    for (int i = 0; i < kCombineThreads / 32; ++i) v += s_red[i][tid];
+    for (int i = 0; i < nwarps; ++i) v += s_red[i][tid];
     s_inv[tid] = 1.0f / sqrtf(v / (float)c.K + c.norm_eps);
   }
   __syncthreads();
-  for (int col = tid * kCols; col < c.K; col += kCombineThreads * kCols) {
+  for (int col = tid * kCols; col < c.K; col += nthreads * kCols) {
     float nw[8];
     norm_w8(c.post_norm_w, col, nw);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -158,10 +160,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t st) {
   if (c.M == 0) return cudaSuccess;
   if (c.top_k > kMaxTopK || c.K % kCols) return cudaErrorInvalidValue;
-  const int chunks = (c.K / kCols + kCombineThreads - 1) / kCombineThreads;
-  const dim3 grid(c.M, c.post_norm_w ? 1 : chunks);
-  combine_kernel<<<grid, kCombineThreads, 0, st>>>(c);
-  return cudaPeekAtLastError();
+  const int chunks = c.K / kCols;
+  if (!c.post_norm_w)  // plain rows: a 2-D grid of 128-thread column blocks
+    return launch_dependent(combine_kernel, dim3(c.M, (chunks + 127) / 128), dim3(128), 0, st, c);
+  int threads = (chunks + 31) / 32 * 32;
+  if (threads > 1024) threads = 1024;
+  return launch_dependent(combine_kernel, dim3(c.M), dim3(threads), 0, st, c);
 }
 
 }  // namespace moe

@@ -99,14 +99,24 @@ struct GemmSmem {
   static_assert(kSA * kAColsPerUnit + kNacc * 2 * BN <= kTmemCols, "TMEM over budget");
 };
 
-// Gated activations in fp32 with the fast exponential and division intrinsics
-// (relative error ~1e-6, far inside the layer's tolerance); a very negative
-// gate gives 0 (its exponential overflows to +inf and the quotient to -0).
+// Gated activations in fp32.  The logistic function is 1/2 + tanh(x/2)/2 on
+// the hardware tanh approximation (one special-function op, relative error
+// ~2^-11, the size of the fp16 rounding the activation gets anyway); it
+// saturates cleanly, so a very negative gate gives 0.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float act_fn(int kind, float g, float u, float alpha, float limit) {
-  if (kind == MOE_ACT_SILU_MUL) return __fdividef(g, 1.0f + __expf(-g)) * u;
+  if (kind == MOE_ACT_SILU_MUL) {
+    const float hg = 0.5f * g;
+    return fmaf(hg, tanh_approx(hg), hg) * u;  // g * sigmoid(g) * u
+  }
   const float gc = fminf(g, limit);
   const float uc = fminf(fmaxf(u, -limit), limit);
-  return __fdividef(gc, 1.0f + __expf(-alpha * gc)) * (uc + 1.0f);
+  const float hg = 0.5f * gc;
+  return fmaf(hg, tanh_approx(alpha * hg), hg) * (uc + 1.0f);  // gc * sigmoid(alpha * gc) * (uc + 1)
 }
 
 struct WorkPlan {
@@ -215,6 +225,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
+  // everything above is on-chip set-up; from here on the kernel reads its
+  // predecessors' outputs
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   const WorkPlan plan = make_plan(g, GATED);
   const int64_t tile_bytes = GATED ? L.tile1_bytes : L.tile2_bytes;

@@ -22,8 +22,7 @@ cudaError_t launch_gemm_instance(const GemmArgs& g, int grid, cudaStream_t st) {
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
-  moe_gemm_kernel<FMT, GATED, BN><<<grid, kGemmThreads, GemmSmem<BN>::kAlloc, st>>>(g);
-  return cudaPeekAtLastError();
+  return launch_dependent(moe_gemm_kernel<FMT, GATED, BN>, dim3(grid), dim3(kGemmThreads), GemmSmem<BN>::kAlloc, st, g);
 }
 
 template <int FMT>
@@ -49,8 +48,8 @@ cudaError_t launch_gemm_small_instance(const GemmArgs& g, int grid, cudaStream_t
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
-  moe_gemm_small_kernel<FMT, GATED, BN><<<grid, kSmallThreads, SmallSmem<BN>::kAlloc, st>>>(g);
-  return cudaPeekAtLastError();
+  return launch_dependent(moe_gemm_small_kernel<FMT, GATED, BN>, dim3(grid), dim3(kSmallThreads),
+                          SmallSmem<BN>::kAlloc, st, g);
 }
 
 template <int FMT>

@@ -260,6 +260,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
   if (warp == 0 && lane == 0)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g.tmap_b)) : "memory");
   __syncthreads();
+  // everything above is on-chip set-up; from here on the kernel reads its
+  // predecessors' outputs
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   const WorkPlan plan = make_plan_small(g, GATED, BN);
   const int64_t tile_bytes = GATED ? L.tile1_bytes : L.tile2_bytes;
