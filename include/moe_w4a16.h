@@ -135,16 +135,19 @@ int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, int num_rou
 int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int block_m);
 
 /* The layer ("013-moe-middle-tiles.py" kernel_fn after alignment; PR #31552
- * fused_marlin_moe):
+ * fused_marlin_moe and the per-expert reference loop of its large-M test):
  *   for every local pair p = (t, j) with expert e:
- *     h = bf16(gs13[e] * x[t] . W13[e]^T + b13[e])            [2N]
- *     a = bf16(act(h[:N], h[N:]))                              [N]
- *     y = bf16(gs2[e] * a . W2[e]^T + b2[e])                   [K]
+ *     h = gs13[e] * x[t] . W13[e]^T + b13[e]                  [2N]
+ *     a = act(h[:N], h[N:])                                    [N]
+ *     y = gs2[e] * a . W2[e]^T + b2[e]                         [K]
  *   out[t] = bf16(rsf * sum_j topk_weights[t,j] * y_(t,j))      (post_norm_w == NULL)
  *   out[t] = bf16(rsf * sum_j topk_weights[t,j] * inv_j * z_j),  z = y * nw,
  *            nw = bf16(fp32(1 + post_norm_w)), inv = 1/sqrt(mean(z^2) + norm_eps)
  *            (_expert_norm_factors / _expert_norm_sum, weight_first)
- * Non-local pairs contribute nothing.
+ * Non-local pairs contribute nothing.  Arithmetic: fp32 accumulation, scales,
+ * bias, activation and combine; the tensor-core operands are fp16 (weights
+ * dequantised exactly, x and a rounded to fp16); a is kept as fp16 and y as
+ * fp32 between the kernels; only out is bf16.
  * Arguments (device unless said): packed from moe_repack_weights for `desc`;
  * x bf16 [M, K]; topk_ids int32 [M, top_k]; topk_weights fp32 [M, top_k];
  * sorted_ids / expert_ids / n_padded from moe_align with the same M, top_k,
