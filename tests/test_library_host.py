@@ -86,6 +86,8 @@ def test_block_m_chooser(lib):
     assert lib.moe_choose_block_m(d, 16, 8, 128) == 8
     assert lib.moe_choose_block_m(d, 256, 8, 128) == 16
     assert lib.moe_choose_block_m(d, 4096, 8, 128) == 128
+    small_k = lib.moe_layer_desc(0, 8, 512, 1024, 128, 0, 1, 1)  # 8 K-stages: 64-token tiles
+    assert lib.moe_choose_block_m(small_k, 2304, 2, 8) == 64
     # monotone in the token count
     prev = 0
     for M in [1, 2, 8, 32, 128, 512, 1024, 4096, 65536]:

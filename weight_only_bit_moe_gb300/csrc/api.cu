@@ -139,7 +139,10 @@ extern "C" int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, 
   if (rows <= 8.0) return 8;
   if (rows <= 16.0) return 16;
   if (rows <= 32.0) return 32;
-  if (rows <= 96.0) return 64;
+  // 128-token tiles keep one accumulator in tensor memory, so the epilogue does
+  // not overlap the next tile's MMAs; below 1024 (16 K-stages per tile) that
+  // epilogue costs more than the 64-token tiles' lower MMA rate
+  if (rows <= 96.0 || desc->hidden < 1024) return 64;
   return 128;
 }
 

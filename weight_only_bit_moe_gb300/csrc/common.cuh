@@ -350,6 +350,32 @@ __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
       : "memory");
 }
+// One 64-K stage of both 128-row halves (8 MMAs: K-steps kk = 0..3, halves
+// h = 0, 1) from the elected lane: D_h (+)= A_h[kk] * B[kk], with A_h[kk] at
+// TMEM column a + 32h + 8kk, B[kk] described by b_desc advanced 32 bytes per
+// K-step and D_h at column d + h * n_cols.  `accumulate` applies to the first
+// K-step; the later ones always accumulate.
+__device__ __forceinline__ void umma_stage_2x4_elect(uint32_t d, uint32_t n_cols, uint32_t a, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 d1, a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "add.u32 d1, %0, %1;\n\t"
+      "add.u32 a1, %2, 32;\n\tadd.u32 a2, %2, 8;\n\tadd.u32 a3, %2, 40;\n\t"
+      "add.u32 a4, %2, 16;\n\tadd.u32 a5, %2, 48;\n\tadd.u32 a6, %2, 24;\n\tadd.u32 a7, %2, 56;\n\t"
+      "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %4, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [d1], [a1], %3, %4, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b1, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [d1], [a3], b1, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b2, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [d1], [a5], b2, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b3, %4, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [d1], [a7], b3, %4, 1;\n\t}" ::"r"(d),
+      "r"(n_cols), "r"(a), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Store 32 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(

@@ -225,9 +225,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
-  // everything above is on-chip set-up; from here on the kernel reads its
-  // predecessors' outputs
-  grid_dependency_wait();
+  // Ordering against the stream predecessors (programmatic launch): this kernel
+  // starts only once its predecessor has passed its own wait, so the alignment
+  // outputs (n_padded, expert_ids, sorted_ids, written two launches earlier) and
+  // the packed weights are complete; the weight producer, the dequant warps and
+  // the MMA warp need no wait.  The activation producer and the epilogue, which
+  // read the predecessor's rows or write counters and outputs, wait first.
   grid_dependents_launch();
 
   const WorkPlan plan = make_plan(g, GATED);
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   } else if (warp == kWarpBProducer) {
     // ------------------------------------------------------------ TMA producer (activation rows)
     if (lane == 0) {
+      grid_dependency_wait();
       uint32_t bk = 0;
       for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
         int b, tile, split, s0, s1;
@@ -316,13 +320,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           if (j < nst) {
             const uint32_t a_t = tmem_base + as * kAColsPerUnit + j * kAColsPerStage;
             const uint64_t bd0 = smem_desc_sw128(b0 + bs * SM::kBUnitBytes + j * kBBytes);
-#pragma unroll
-            for (int kk = 0; kk < kStageK / 16; ++kk) {
-              const uint64_t bd = bd0 + (uint64_t)(2 * kk);  // start address advances 32 bytes per K=16 step
-              const uint32_t acc = (s > s0 || j > 0 || kk > 0) ? 1u : 0u;
-              umma_f16_tmem_a_elect(d0, a_t + kk * 8, bd, idesc, acc);
-              umma_f16_tmem_a_elect(d0 + BN, a_t + 32 + kk * 8, bd, idesc, acc);
-            }
+            // 4 K-steps x 2 halves; the B start address advances 32 bytes per K-step
+            umma_stage_2x4_elect(d0, BN, a_t, bd0, idesc, (s > s0 || j > 0) ? 1u : 0u);
           }
         }
         umma_commit_elect(&a_empty[as]);
@@ -426,6 +425,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ epilogue warps
+    grid_dependency_wait();
     const int q = warp & 3;            // TMEM lane quarter
     const int hr = q * 32 + lane;      // row within each 128-row half
     const int et = threadIdx.x - kWarpEpi0 * 32;  // 0..255

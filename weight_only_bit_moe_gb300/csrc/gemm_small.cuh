@@ -260,9 +260,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
   if (warp == 0 && lane == 0)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g.tmap_b)) : "memory");
   __syncthreads();
-  // everything above is on-chip set-up; from here on the kernel reads its
-  // predecessors' outputs
-  grid_dependency_wait();
+  // Ordering against the stream predecessors (programmatic launch): this kernel
+  // starts only once its predecessor has passed its own wait, so the alignment
+  // outputs (n_padded, expert_ids, sorted_ids, written two launches earlier) and
+  // the packed weights are complete and the producer streams weights at once.
+  // The activation rows, the split-K counters and the outputs belong to the
+  // predecessor: every thread that touches them waits first.
   grid_dependents_launch();
 
   const WorkPlan plan = make_plan_small(g, GATED, BN);
@@ -273,6 +276,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      // The first ring's worth of weight copies go out before the wait on the
+      // predecessor; their activation boxes (the predecessor's output) follow it.
+      // Each slot's barrier expects both byte counts from the start.
+      int pend_row[kSlots], pend_stage[kSlots];
+      uint32_t npend = 0;
+      bool waited = false;
       uint32_t ck = 0;
       for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
         int b, tile, split, s0, s1;
@@ -283,6 +292,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
           const int c1 = min(c0 + kSmallChunk, s1);
           const int slot = ck % kSlots;
+          if (!waited && ck == (uint32_t)kSlots) {
+            grid_dependency_wait();
+            waited = true;
+            for (uint32_t i = 0; i < npend; ++i)
+              tma_tile3d(smem_u32(smem + i * SM::kSlotBytes + kSmallWBytes), &g.tmap_b, 0, pend_row[i], pend_stage[i],
+                         &full[i]);
+          }
           mbar_wait(&empty[slot], ((ck / kSlots) + 1) & 1, abort_flag, g.status);
           // c0 and c1 lie on scale-period boundaries
           const int64_t off0 = (int64_t)(c0 / PackedFmt<FMT>::kPeriod) * PackedFmt<FMT>::kPeriodBytes;
@@ -290,8 +306,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
           unsigned char* dst = smem + slot * SM::kSlotBytes;
           mbar_arrive_expect_tx(&full[slot], wbytes + SM::kBBytes);
           bulk_g2s(dst, tb + off0, wbytes, &full[slot], pol);
-          tma_tile3d(smem_u32(dst + kSmallWBytes), &g.tmap_b, 0, b * g.block_m, c0, &full[slot]);
+          if (waited) {
+            tma_tile3d(smem_u32(dst + kSmallWBytes), &g.tmap_b, 0, b * g.block_m, c0, &full[slot]);
+          } else {  // ck < kSlots: slot == ck
+            pend_row[npend] = b * g.block_m;
+            pend_stage[npend] = c0;
+            ++npend;
+          }
         }
+      }
+      if (!waited) {
+        grid_dependency_wait();
+        for (uint32_t i = 0; i < npend; ++i)
+          tma_tile3d(smem_u32(smem + i * SM::kSlotBytes + kSmallWBytes), &g.tmap_b, 0, pend_row[i], pend_stage[i],
+                     &full[i]);
       }
       // leave no copy in flight
       for (uint32_t i = 0; i < (uint32_t)kSlots && i < ck; ++i) {
@@ -303,6 +331,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     }
   } else {
     // ------------------------------------------------------------ consumer warps
+    grid_dependency_wait();
     const int cw = warp - 1;
     const int gq = lane >> 2, tq = lane & 3;
     SmallFrag<NT> F;
@@ -417,7 +446,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
           for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
-        for (int sp = 0; sp < plan.S; ++sp)
+#pragma unroll 4
+        for (int sp = 0; sp < plan.S; ++sp)  // several slices' loads in flight at once
 #pragma unroll
           for (int i = 0; i < kSmallMI; ++i)
 #pragma unroll
