@@ -169,3 +169,51 @@ def test_forward_full_sampled(name, M):
     ref = bf16_to_f32(oracle.forward_workload(wl, W, X, tokens=toks))
     check_close(out.float().cpu().numpy()[toks], ref, f"{name} M={M}")
     assert layer.status() == 0
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_forward_routed_scaling_factor():
+    wl = GPU_SMALL["int4-bias-small"]
+    W = wk.make_weights(wl, 91)
+    X = wk.make_batch(wl, 19, 92)
+    out = run_layer(_layer(W), wl, X, routed_scaling_factor=2.5)
+    ref = bf16_to_f32(oracle.forward_workload(wl, W, X, rsf=2.5))
+    check_close(out.float().cpu().numpy(), ref, "rsf=2.5")
+
+
+def test_forward_top_k_16():
+    # the combine's largest slot count; 16 distinct experts per token
+    wl = dataclasses.replace(GPU_SMALL["int4-zipf-small"], E=32, top_k=16, routing="uniform")
+    W = wk.make_weights(wl, 101)
+    X = wk.make_batch(wl, 23, 102)
+    out = run_layer(_layer(W), wl, X)
+    check_close(out.float().cpu().numpy(), bf16_to_f32(oracle.forward_workload(wl, W, X)), "top_k=16")
+
+
+@pytest.mark.parametrize("B", [8, 64, 128])
+def test_forward_all_tokens_on_two_experts(B):
+    # one extreme of routing skew: every token picks experts 3 and 5, so two
+    # experts own many blocks and the rest none
+    wl = GPU_SMALL["int4-zipf-small"]
+    W = wk.make_weights(wl, 111)
+    X = wk.make_batch(wl, 300, 112)
+    ids = np.tile(np.array([[3, 5]], dtype=np.int32), (300, 1))[:, : wl.top_k]
+    if wl.top_k > 2:
+        ids = np.concatenate([ids, np.tile(np.arange(6, 6 + wl.top_k - 2, dtype=np.int32), (300, 1))], axis=1)
+    X = wk.BatchInputs(X.x, ids, X.topk_weights, X.post_norm_w)
+    out = run_layer(_layer(W), wl, X, block_m=B)
+    toks = sample_tokens(300, 24, seed=B)
+    ref = bf16_to_f32(oracle.forward_workload(wl, W, X, tokens=toks))
+    check_close(out.float().cpu().numpy()[toks], ref, f"two hot experts, block_m={B}")
+
+
+@pytest.mark.parametrize("fmt,K,N", [("nvfp4", 64, 16), ("mxfp4", 64, 32), ("int4", 128, 128)])
+def test_forward_smallest_shapes(fmt, K, N):
+    # one K-stage, the smallest intermediate each format accepts, a ragged tile
+    wl = wk.Workload(f"{fmt}-min", fmt, K=K, N=N, E=3, top_k=2, Ms=(7,))
+    W = wk.make_weights(wl, 121)
+    X = wk.make_batch(wl, 7, 122)
+    for B in (8, 64):
+        out = run_layer(_layer(W), wl, X, block_m=B)
+        check_close(out.float().cpu().numpy(), bf16_to_f32(oracle.forward_workload(wl, W, X)), f"{fmt} K={K} N={N} B={B}")
