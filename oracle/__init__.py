@@ -29,7 +29,7 @@ _lock = threading.Lock()
 _lib = None
 
 FMT_CODES = {"int4": 0, "mxfp4": 1, "nvfp4": 2}
-ACT_CODES = {"silu_mul": 0, "sigmoid_alpha": 1}
+ACT_CODES = {"silu_mul": 0, "sigmoid_alpha": 1, "relu2": 2}
 
 
 def build(force: bool = False) -> str:
@@ -48,7 +48,7 @@ class _Layer(ctypes.Structure):
                 ("inter", ctypes.c_int), ("group", ctypes.c_int), ("interleaved", ctypes.c_int),
                 ("w13", ctypes.c_void_p), ("w13_s", ctypes.c_void_p), ("w13_gs", ctypes.c_void_p),
                 ("b13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w2_s", ctypes.c_void_p),
-                ("w2_gs", ctypes.c_void_p), ("b2", ctypes.c_void_p)]
+                ("w2_gs", ctypes.c_void_p), ("b2", ctypes.c_void_p), ("gated", ctypes.c_int)]
 
 
 class _Batch(ctypes.Structure):
@@ -167,7 +167,8 @@ def _structs(W, X, expert_base, act, alpha, limit, rsf, norm_eps, post_norm, kee
 
     layer = _Layer(FMT_CODES[W.fmt], W.E, W.K, W.N, W.group, int(W.interleaved),
                    c(W.w13, np.uint8), c(W.w13_s), c(W.w13_gs, np.float32), c(W.b13, np.uint16),
-                   c(W.w2, np.uint8), c(W.w2_s), c(W.w2_gs, np.float32), c(W.b2, np.uint16))
+                   c(W.w2, np.uint8), c(W.w2_s), c(W.w2_gs, np.float32), c(W.b2, np.uint16),
+                   int(getattr(W, "gated", True)))
     pnw = X.post_norm_w if post_norm else None
     b = _Batch(M, k, expert_base, ACT_CODES[act], alpha, limit, rsf, norm_eps,
                c(X.x, np.uint16), c(X.topk_ids, np.int32), c(X.topk_weights, np.float32),
@@ -200,11 +201,13 @@ def forward(weights, batch, *, expert_base: int = 0, act: str = "silu_mul", alph
 
 def ffn_pair(weights, batch, e: int, t: int, *, expert_base: int = 0, act: str = "silu_mul",
              alpha: float = 1.702, limit: float = float("inf")):
-    """(h[2N], a[N], y[K]) of token t on local expert e, in fp64."""
+    """(h[R], a[N], y[K]) of token t on local expert e, in fp64; R = 2N for
+    gated experts, N for non-gated ones."""
     keep = []
     layer, b = _structs(weights, batch, expert_base, act, alpha, limit, 1.0, 1e-8, False, keep)
     N, K = weights.N, weights.K
-    h, a, y = np.empty(2 * N), np.empty(N), np.empty(K)
+    R = 2 * N if getattr(weights, "gated", True) else N
+    h, a, y = np.empty(R), np.empty(N), np.empty(K)
     if lib().orc_ffn_pair(ctypes.byref(layer), ctypes.byref(b), e, t, _ptr(h), _ptr(a), _ptr(y)) != 0:
         raise ValueError("oracle ffn_pair rejected its arguments")
     return h, a, y

@@ -31,6 +31,9 @@
  *               act = silu(g)*u (silu_and_mul) or
  *                     g' = min(g, L), u' = clamp(u,-L,L), g'*sigmoid(alpha*g')*(u'+1)
  *               (swiglu_gpt_oss_sigmoid_alpha_contiguous of PR #28231);
+ *               non-gated experts (w1 has N rows, is_gated=False): a = relu(h)^2
+ *               (activation="relu2" of the PR #31552 large-M test, whose reference
+ *               loop computes torch.square(torch.relu(intermediate)));
  *   combine     out[t] = bf16(rsf * sum_j w[t,j] * y[t,j]) over local slots
  *               (the per-expert reference loop of the PR #31552 test), or with the
  *               post-expert norm of "013-moe-middle-tiles.py" (_expert_norm_factors,
@@ -54,7 +57,7 @@
 #endif
 
 enum { ORC_INT4 = 0, ORC_MXFP4 = 1, ORC_NVFP4 = 2 };
-enum { ORC_SILU_MUL = 0, ORC_SIGMOID_ALPHA = 1 };
+enum { ORC_SILU_MUL = 0, ORC_SIGMOID_ALPHA = 1, ORC_RELU2 = 2 };
 
 /* ------------------------------------------------------------------ formats */
 
@@ -216,14 +219,15 @@ int orc_align(const int32_t* topk_ids, int M, int top_k, int base, int num_exper
 
 typedef struct {
     int fmt, num_experts, hidden, inter, group, interleaved;
-    const uint8_t* w13;   /* [E, 2N, K/2] */
-    const void* w13_s;    /* [E, 2N, K/g] */
+    const uint8_t* w13;   /* [E, R, K/2], R = 2N gated (gate rows then up rows), N non-gated */
+    const void* w13_s;    /* [E, R, K/g] */
     const float* w13_gs;  /* [E] or NULL */
-    const uint16_t* b13;  /* [E, 2N] bf16 or NULL */
+    const uint16_t* b13;  /* [E, R] bf16 or NULL */
     const uint8_t* w2;    /* [E, K, N/2] */
     const void* w2_s;     /* [E, K, N/g] */
     const float* w2_gs;   /* [E] or NULL */
     const uint16_t* b2;   /* [E, K] bf16 or NULL */
+    int gated;            /* 1: gate and up rows, act on (gate, up); 0: N rows, relu^2 */
 } orc_layer;
 
 typedef struct {
@@ -238,6 +242,7 @@ typedef struct {
 static double round_bf16(double v) { return orc_bf16_value(orc_bf16_round(v)); }
 
 static double activation(int act, double g, double u, double alpha, double limit) {
+    if (act == ORC_RELU2) return g > 0.0 ? g * g : 0.0;  /* non-gated: u unused */
     if (act == ORC_SILU_MUL) return g / (1.0 + exp(-g)) * u;
     double gc = g < limit ? g : limit;
     double uc = u > limit ? limit : (u < -limit ? -limit : u);
@@ -247,21 +252,22 @@ static double activation(int act, double g, double u, double alpha, double limit
 /* y[K] of one pair whose expert weights are already dequantised. */
 static void ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, const float* W13,
                      const float* W2, double* h, double* a, double* y) {
-    const int K = L->hidden, N = L->inter;
+    const int K = L->hidden, N = L->inter, R = L->gated ? 2 * N : N;
     const uint16_t* xr = X->x + (long)t * K;
     double gs13 = L->w13_gs ? (double)L->w13_gs[e] : 1.0;
     double gs2 = L->w2_gs ? (double)L->w2_gs[e] : 1.0;
 #pragma omp parallel for schedule(static)
-    for (int r = 0; r < 2 * N; ++r) {
+    for (int r = 0; r < R; ++r) {
         const float* wr = W13 + (long)r * K;
         double acc = 0.0;
         for (int c = 0; c < K; ++c) acc += orc_bf16_value(xr[c]) * (double)wr[c];
-        long br = L->interleaved ? (long)2 * (r % N) + (r / N) : r;
-        double b = L->b13 ? orc_bf16_value(L->b13[(long)e * 2 * N + br]) : 0.0;
+        long br = (L->gated && L->interleaved) ? (long)2 * (r % N) + (r / N) : r;
+        double b = L->b13 ? orc_bf16_value(L->b13[(long)e * R + br]) : 0.0;
         h[r] = gs13 * acc + b;
     }
     for (int n = 0; n < N; ++n)
-        a[n] = activation(X->act, h[n], h[N + n], X->alpha, X->limit);
+        a[n] = L->gated ? activation(X->act, h[n], h[N + n], X->alpha, X->limit)
+                        : activation(ORC_RELU2, h[n], 0.0, X->alpha, X->limit);
 #pragma omp parallel for schedule(static)
     for (int c = 0; c < K; ++c) {
         const float* wr = W2 + (long)c * N;
@@ -282,14 +288,17 @@ static void ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, const
 int orc_forward(const orc_layer* L, const orc_batch* X, const int32_t* tokens, int n_tokens,
                 uint16_t* out_bf16, double* out_acc) {
     const int K = L->hidden, N = L->inter, E = L->num_experts, k = X->top_k;
+    const int R = L->gated ? 2 * N : N;  /* rows of w13 */
     if (K <= 0 || N <= 0 || E <= 0 || k <= 0 || L->group <= 0) return -1;
+    if (!L->gated && X->act != ORC_RELU2) return -1;
+    if (L->gated && X->act == ORC_RELU2) return -1;
     if (K % L->group || N % L->group || K % 2 || N % 2) return -1;
     double* acc_out = (double*)calloc((size_t)n_tokens * K, sizeof(double));
     double* nsq = (double*)calloc((size_t)n_tokens * k, sizeof(double));
-    float* W13 = (float*)malloc(sizeof(float) * (size_t)2 * N * K);
+    float* W13 = (float*)malloc(sizeof(float) * (size_t)R * K);
     float* W2 = (float*)malloc(sizeof(float) * (size_t)K * N);
-    int32_t* rmap = (int32_t*)malloc(sizeof(int32_t) * 2 * (size_t)N);
-    double* h = (double*)malloc(sizeof(double) * 2 * (size_t)N);
+    int32_t* rmap = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
+    double* h = (double*)malloc(sizeof(double) * (size_t)R);
     double* a = (double*)malloc(sizeof(double) * (size_t)N);
     double* y = (double*)malloc(sizeof(double) * (size_t)K);
     double* nw = (double*)malloc(sizeof(double) * (size_t)K);
@@ -297,8 +306,8 @@ int orc_forward(const orc_layer* L, const orc_batch* X, const int32_t* tokens, i
         free(acc_out); free(nsq); free(W13); free(W2); free(rmap); free(h); free(a); free(y); free(nw);
         return -1;
     }
-    for (int r = 0; r < 2 * N; ++r)  /* logical row r -> stored row */
-        rmap[r] = L->interleaved ? 2 * (r % N) + (r / N) : r;
+    for (int r = 0; r < R; ++r)  /* logical row r -> stored row */
+        rmap[r] = (L->gated && L->interleaved) ? 2 * (r % N) + (r / N) : r;
     if (X->post_norm_w)
         for (int c = 0; c < K; ++c) {
             float s = (float)(1.0 + orc_bf16_value(X->post_norm_w[c]));  /* fp32 add, as torch */
@@ -311,8 +320,8 @@ int orc_forward(const orc_layer* L, const orc_batch* X, const int32_t* tokens, i
             for (int j = 0; j < k; ++j)
                 if (X->topk_ids[(long)tokens[i] * k + j] - X->expert_base == e) { touched = 1; break; }
         if (!touched) continue;
-        orc_dequant(L->fmt, L->w13 + (long)e * 2 * N * (K / 2),
-                    (const uint8_t*)L->w13_s + (long)e * 2 * N * (K / L->group) * sb, 2 * N, K, L->group,
+        orc_dequant(L->fmt, L->w13 + (long)e * R * (K / 2),
+                    (const uint8_t*)L->w13_s + (long)e * R * (K / L->group) * sb, R, K, L->group,
                     rmap, W13);
         orc_dequant(L->fmt, L->w2 + (long)e * K * (N / 2),
                     (const uint8_t*)L->w2_s + (long)e * K * (N / L->group) * sb, K, N, L->group, NULL, W2);
@@ -354,16 +363,16 @@ int orc_num_threads(void) {
 /* Intermediates of one pair (token t on local expert e): h[2N], a[N], y[K]
  * as the forward computes them.  Returns 0 or -1. */
 int orc_ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, double* h, double* a, double* y) {
-    const int K = L->hidden, N = L->inter;
+    const int K = L->hidden, N = L->inter, R = L->gated ? 2 * N : N;
     if (e < 0 || e >= L->num_experts || t < 0 || t >= X->M) return -1;
-    float* W13 = (float*)malloc(sizeof(float) * (size_t)2 * N * K);
+    float* W13 = (float*)malloc(sizeof(float) * (size_t)R * K);
     float* W2 = (float*)malloc(sizeof(float) * (size_t)K * N);
-    int32_t* rmap = (int32_t*)malloc(sizeof(int32_t) * 2 * (size_t)N);
+    int32_t* rmap = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
     if (!W13 || !W2 || !rmap) { free(W13); free(W2); free(rmap); return -1; }
-    for (int r = 0; r < 2 * N; ++r) rmap[r] = L->interleaved ? 2 * (r % N) + (r / N) : r;
+    for (int r = 0; r < R; ++r) rmap[r] = (L->gated && L->interleaved) ? 2 * (r % N) + (r / N) : r;
     const long sb = scale_bytes(L->fmt);
-    orc_dequant(L->fmt, L->w13 + (long)e * 2 * N * (K / 2),
-                (const uint8_t*)L->w13_s + (long)e * 2 * N * (K / L->group) * sb, 2 * N, K, L->group, rmap, W13);
+    orc_dequant(L->fmt, L->w13 + (long)e * R * (K / 2),
+                (const uint8_t*)L->w13_s + (long)e * R * (K / L->group) * sb, R, K, L->group, rmap, W13);
     orc_dequant(L->fmt, L->w2 + (long)e * K * (N / 2),
                 (const uint8_t*)L->w2_s + (long)e * K * (N / L->group) * sb, K, N, L->group, NULL, W2);
     ffn_pair(L, X, e, t, W13, W2, h, a, y);

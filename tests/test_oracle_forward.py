@@ -70,8 +70,9 @@ def dense_reference(wl, W, X, rsf=1.0):
     """Every expert on every token, then select; fp64 throughout, the caller
     rounds the output to bf16."""
     E, K, N = W.E, W.K, W.N
-    W13 = decode_matrix(W.fmt, W.w13, W.w13_s, W.group)  # [E, 2N, K]
-    b13 = bf16v(W.b13) if W.b13 is not None else np.zeros((E, 2 * N))
+    R = 2 * N if W.gated else N
+    W13 = decode_matrix(W.fmt, W.w13, W.w13_s, W.group)  # [E, R, K]
+    b13 = bf16v(W.b13) if W.b13 is not None else np.zeros((E, R))
     if W.interleaved:  # stored rows g0,u0,g1,u1,... -> gate block then up block
         W13 = np.concatenate([W13[:, 0::2], W13[:, 1::2]], axis=1)
         b13 = np.concatenate([b13[:, 0::2], b13[:, 1::2]], axis=1)
@@ -85,7 +86,9 @@ def dense_reference(wl, W, X, rsf=1.0):
     for e in range(E):
         h = gs13[e] * (x @ W13[e].T) + b13[e]
         g, u = h[:, :N], h[:, N:]
-        if wl.act == "silu_mul":
+        if not W.gated:
+            a = np.square(np.maximum(h, 0.0))
+        elif wl.act == "silu_mul":
             a = g / (1 + np.exp(-g)) * u
         else:
             gc = np.minimum(g, wl.limit)
@@ -118,6 +121,9 @@ SMALL = {
     "nvfp4-ep-small": dataclasses.replace(wk.WORKLOADS["nvfp4-ep-norm"], K=64, N=48, E=4, E_global=16,
                                           expert_base=4, Ms=(12,)),
     "int4-zipf-small": dataclasses.replace(wk.WORKLOADS["int4-skew"], K=256, N=128, E=16, Ms=(10,)),
+    "int4-relu2-small": dataclasses.replace(wk.WORKLOADS["int4-relu2"], K=256, N=256, E=4, Ms=(11,)),
+    "nvfp4-relu2-small": dataclasses.replace(wk.WORKLOADS["int4-relu2"], fmt="nvfp4", K=64, N=48, E=4,
+                                             Ms=(9,)),
 }
 
 
@@ -141,25 +147,26 @@ def test_dense_bruteforce(orc, name):
 
 
 @pytest.mark.parametrize("fmt", ["int4", "mxfp4", "nvfp4"])
-@pytest.mark.parametrize("act", ["silu_mul", "sigmoid_alpha"])
+@pytest.mark.parametrize("act", ["silu_mul", "sigmoid_alpha", "relu2"])
 def test_closed_form_unit_scales(orc, fmt, act):
     """Unit scales, zero bias, every w13 code c1, every w2 code c2 and x in
-    {-1/8, 0, 1/8}: h = v1*S_t on every row, a = act(h, h), y = v2*N*a,
-    out_t = bf16(rsf * sum_j w_tj * y_t)."""
+    {-1/8, 0, 1/8}: h = v1*S_t on every row, a = act(h, h) (relu(h)^2 for the
+    non-gated experts), y = v2*N*a, out_t = bf16(rsf * sum_j w_tj * y_t)."""
     K, N, E, k, M = 128, 128, 3, 2, 6
     group = {"int4": 128, "mxfp4": 32, "nvfp4": 16}[fmt]
-    wl = wk.Workload("closed", fmt, K=K, N=N, E=E, top_k=k, Ms=(M,), act=act)
+    gated = act != "relu2"
+    R = 2 * N if gated else N
     c1, c2 = (11, 6) if fmt == "int4" else (3, 10)    # int4: 3 and -2; e2m1: 1.5 and -1.0
     v1 = c1 - 8.0 if fmt == "int4" else E2M1[c1]
     v2 = c2 - 8.0 if fmt == "int4" else E2M1[c2]
     unit = {"int4": np.uint16(0x3F80), "mxfp4": np.uint8(127), "nvfp4": np.uint8(0x38)}[fmt]
     W = wk.LayerWeights(fmt, E, K, N, group, False,
-                        np.full((E, 2 * N, K // 2), c1 | (c1 << 4), np.uint8),
-                        np.full((E, 2 * N, K // group), unit), np.ones(E, np.float32) if fmt == "nvfp4" else None,
+                        np.full((E, R, K // 2), c1 | (c1 << 4), np.uint8),
+                        np.full((E, R, K // group), unit), np.ones(E, np.float32) if fmt == "nvfp4" else None,
                         None,
                         np.full((E, K, N // 2), c2 | (c2 << 4), np.uint8),
                         np.full((E, K, N // group), unit), np.ones(E, np.float32) if fmt == "nvfp4" else None,
-                        None)
+                        None, gated=gated)
     rng = np.random.default_rng(3)
     xv = rng.integers(-1, 2, size=(M, K)) / 8.0
     x = torch.from_numpy(xv.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
@@ -172,7 +179,9 @@ def test_closed_form_unit_scales(orc, fmt, act):
     for t in range(M):
         S = xv[t].sum()
         h = v1 * S
-        if act == "silu_mul":
+        if act == "relu2":
+            a = max(h, 0.0) ** 2
+        elif act == "silu_mul":
             a = h / (1 + math.exp(-h)) * h
         else:
             a = h / (1 + math.exp(-1.702 * h)) * (h + 1)
@@ -181,6 +190,39 @@ def test_closed_form_unit_scales(orc, fmt, act):
         # fp64 evaluation order differs from the oracle's sums only in the last bits
         np.testing.assert_allclose(got_acc[t], expect, rtol=1e-12, atol=1e-300)
         assert np.all(got[t] == float(rne_bf16(np.array(expect)))), (t, got[t][:4], expect)
+
+
+def test_relu2_rejects_gated_mismatch(orc):
+    """The non-gated layout goes only with relu2, and relu2 only with it."""
+    wl, W, X = make_small("int4-relu2-small")
+    with pytest.raises(ValueError):
+        orc.forward(W, X, act="silu_mul")
+    wg, Wg, Xg = make_small("int4-bias-small")
+    with pytest.raises(ValueError):
+        orc.forward(Wg, Xg, act="relu2")
+
+
+def test_relu2_negative_rows_give_zero(orc):
+    """relu2 clips: with every w13 row negated the intermediates of rows whose
+    h was positive become zero, so the two outputs are y(+W) and y(-W), whose
+    activations a+ and a- have disjoint supports and satisfy a+ + a- = h^2."""
+    wl, W, X = make_small("int4-relu2-small")
+    # negate each int4 code: q -> 16 - q maps (q - 8) to -(q - 8); code 0 (-8) has no
+    # negation, so it is first replaced by 8 (zero) in both layers
+    q_lo, q_hi = W.w13 & 15, W.w13 >> 4
+    ok = (q_lo != 0) & (q_hi != 0)
+    lo = np.where(q_lo == 0, 8, q_lo)
+    hi = np.where(q_hi == 0, 8, q_hi)
+    Wp = dataclasses.replace(W, w13=(lo | (hi << 4)).astype(np.uint8), b13=None)
+    Wn = dataclasses.replace(W, w13=(((16 - lo) & 15) | (((16 - hi) & 15) << 4)).astype(np.uint8), b13=None)
+    assert ok.mean() > 0.8
+    for e, t in [(0, 0), (1, 3), (3, 7)]:
+        hp, ap, _ = orc.ffn_pair(Wp, X, e, t, act="relu2")
+        hn, an, _ = orc.ffn_pair(Wn, X, e, t, act="relu2")
+        np.testing.assert_allclose(hn, -hp, rtol=0, atol=1e-12)
+        assert np.all((ap == 0) | (an == 0))
+        np.testing.assert_allclose(ap + an, hp * hp, rtol=1e-12, atol=1e-300)
+        assert (ap > 0).any() and (an > 0).any()
 
 
 @pytest.mark.parametrize("name", ["int4-bias-small", "nvfp4-ep-small", "mxfp4-alpha-small"])

@@ -21,6 +21,9 @@ The five workloads follow the problem statements on the source pages:
                       ``Config``, ``Inputs``).
 * ``int4-skew``       int4 K=4096, N=1536, E=128, top_k=8 with uniform or Zipf(1.2)
                       routing.
+* ``int4-relu2``      the PR #31552 test shape as that test writes it: non-gated
+                      experts (w1 [E, N, K]) with relu(h)^2, x = randn/10, bias
+                      = randn/100.
 
 Distributions not fixed by the pages (stated here once): x ~ N(0,1) in bf16;
 routing ids distinct per token (Gumbel-top-k over the routing distribution);
@@ -42,6 +45,7 @@ FMT_NVFP4 = "nvfp4"  # E2M1 codes, E4M3 scale per 16, fp32 global scale per expe
 
 ACT_SILU_MUL = "silu_mul"
 ACT_SIGMOID_ALPHA = "sigmoid_alpha"
+ACT_RELU2 = "relu2"  # non-gated experts: relu(h)^2
 
 GROUP = {FMT_INT4: 128, FMT_MXFP4: 32, FMT_NVFP4: 16}
 
@@ -66,6 +70,8 @@ class Workload:
     norm_eps: float = 1e-8
     routing: str = "uniform"       # "uniform" | "zipf"
     zipf_s: float = 1.2
+    gated: bool = True             # False: w1 has N rows and act is relu2
+    x_scale: float = 1.0           # x ~ N(0, x_scale^2)
 
     @property
     def group(self) -> int:
@@ -90,10 +96,14 @@ WORKLOADS = {
                           Ms=(1, 16, 256, 4096), routing="zipf"),
     "int4-uniform": Workload("int4-uniform", FMT_INT4, K=4096, N=1536, E=128, top_k=8,
                              Ms=(1, 16, 256, 4096), routing="uniform"),
+    # the large-M schedule test of "Marlin MoE kernel occupancy ..." (PR #31552)
+    # as it is written: non-gated relu2 experts, x = randn/10, bias = randn/100
+    "int4-relu2": Workload("int4-relu2", FMT_INT4, K=512, N=1024, E=8, top_k=2,
+                           Ms=(123, 2304), bias_std=0.01, gated=False, act=ACT_RELU2, x_scale=0.1),
 }
 
 WORKLOAD_INDEX = {"tiny-int4": 0, "int4-bias": 1, "mxfp4-alpha": 2, "nvfp4-ep-norm": 3,
-                  "int4-skew": 4, "int4-uniform": 5}
+                  "int4-skew": 4, "int4-uniform": 5, "int4-relu2": 6}
 
 
 def weight_seed(name: str) -> int:
@@ -126,10 +136,11 @@ def to_e4m3_bits(a: np.ndarray) -> np.ndarray:
 class LayerWeights:
     """Raw expert weights, in the layout the pages' checkpoints use.
 
-    w13    uint8 [E, 2N, K/2]  two 4-bit codes per byte, low nibble = even index
-    w13_s  [E, 2N, K/g]        uint16 bf16 bits (int4) | uint8 E8M0 (mxfp4) | uint8 E4M3 (nvfp4)
+    w13    uint8 [E, R, K/2]   two 4-bit codes per byte, low nibble = even index;
+                               R = 2N (gate and up) or N for non-gated experts
+    w13_s  [E, R, K/g]         uint16 bf16 bits (int4) | uint8 E8M0 (mxfp4) | uint8 E4M3 (nvfp4)
     w13_gs float32 [E]         nvfp4 only (one global scale per expert, gate and up)
-    b13    uint16 bf16 bits [E, 2N] or None
+    b13    uint16 bf16 bits [E, R] or None
     w2     uint8 [E, K, N/2];  w2_s [E, K, N/g];  w2_gs float32 [E];  b2 uint16 [E, K] or None
     When ``interleaved`` the 2N rows of w13 (and its scale and bias rows) are
     gate0, up0, gate1, up1, ...; otherwise gate rows [0, N) then up rows [N, 2N).
@@ -148,6 +159,7 @@ class LayerWeights:
     w2_s: np.ndarray
     w2_gs: Optional[np.ndarray]
     b2: Optional[np.ndarray]
+    gated: bool = True
 
 
 def _scales(rng: np.random.Generator, fmt: str, shape) -> np.ndarray:
@@ -164,9 +176,10 @@ def _scales(rng: np.random.Generator, fmt: str, shape) -> np.ndarray:
 def make_weights(wl: Workload, seed: int) -> LayerWeights:
     rng = np.random.Generator(np.random.PCG64(seed))
     E, K, N, g = wl.E, wl.K, wl.N, wl.group
+    R = 2 * N if wl.gated else N  # rows of w13
     # every code value equally likely: uniform bytes give uniform nibbles
-    w13 = rng.integers(0, 256, size=(E, 2 * N, K // 2), dtype=np.uint8)
-    w13_s = _scales(rng, wl.fmt, (E, 2 * N, K // g))
+    w13 = rng.integers(0, 256, size=(E, R, K // 2), dtype=np.uint8)
+    w13_s = _scales(rng, wl.fmt, (E, R, K // g))
     w2 = rng.integers(0, 256, size=(E, K, N // 2), dtype=np.uint8)
     w2_s = _scales(rng, wl.fmt, (E, K, N // g))
     w13_gs = w2_gs = None
@@ -175,10 +188,10 @@ def make_weights(wl: Workload, seed: int) -> LayerWeights:
         w2_gs = rng.uniform(0.008, 0.012, size=E).astype(np.float32)
     b13 = b2 = None
     if wl.bias_std > 0:
-        b13 = to_bf16_bits(rng.normal(0.0, wl.bias_std, size=(E, 2 * N)).astype(np.float32))
+        b13 = to_bf16_bits(rng.normal(0.0, wl.bias_std, size=(E, R)).astype(np.float32))
         b2 = to_bf16_bits(rng.normal(0.0, wl.bias_std, size=(E, K)).astype(np.float32))
     return LayerWeights(wl.fmt, E, K, N, g, wl.interleaved, w13, w13_s, w13_gs, b13,
-                        w2, w2_s, w2_gs, b2)
+                        w2, w2_s, w2_gs, b2, gated=wl.gated)
 
 
 # ---------------------------------------------------------------- per-batch inputs
@@ -205,7 +218,7 @@ def routing_log_probs(wl: Workload) -> np.ndarray:
 
 def make_batch(wl: Workload, M: int, seed: int) -> BatchInputs:
     rng = np.random.Generator(np.random.PCG64(seed))
-    x = to_bf16_bits(rng.standard_normal((M, wl.K), dtype=np.float32))
+    x = to_bf16_bits(rng.standard_normal((M, wl.K), dtype=np.float32) * np.float32(wl.x_scale))
     logp = routing_log_probs(wl)
     # Gumbel-top-k: k distinct ids per token, drawn without replacement from p
     gumbel = -np.log(-np.log(rng.uniform(1e-12, 1.0, size=(M, wl.n_ids))))
