@@ -37,7 +37,7 @@ DEFAULT_WORKLOAD, DEFAULT_M = "int4-bias", 2304
 SWEEP = [("int4-bias", 123), ("int4-bias", 2304), ("mxfp4-alpha", 1), ("mxfp4-alpha", 32), ("mxfp4-alpha", 1024),
          ("nvfp4-ep-norm", 1), ("nvfp4-ep-norm", 8), ("nvfp4-ep-norm", 64), ("nvfp4-ep-norm", 512),
          ("int4-skew", 1), ("int4-skew", 16), ("int4-skew", 256), ("int4-skew", 4096), ("int4-uniform", 16),
-         ("int4-uniform", 256), ("int4-uniform", 4096)]
+         ("int4-uniform", 256), ("int4-uniform", 4096), ("int4-relu2", 123), ("int4-relu2", 2304)]
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 
 
@@ -68,7 +68,7 @@ def algorithmic(wl, W, X):
     io = X.x.nbytes + M * wl.K * 2 + X.topk_ids.nbytes + X.topk_weights.nbytes
     if wl.post_norm:
         io += wl.K * 2
-    f1 = 2.0 * P * wl.K * 2 * wl.N
+    f1 = 2.0 * P * wl.K * (2 if wl.gated else 1) * wl.N  # gate and up rows, or h rows only
     f2 = 2.0 * P * wl.N * wl.K
     return {"bytes": w13 + w2 + io, "bytes_gemm1": w13 + X.x.nbytes, "bytes_gemm2": w2,
             "flops": f1 + f2, "flops_gemm1": f1, "flops_gemm2": f2, "pairs": P, "touched": nt}
@@ -305,7 +305,8 @@ def run_ours(args, rank: int, world: int):
     dom = "gemm1" if g1 >= g2 else "gemm2"
     dom_ms = g1 if dom == "gemm1" else g2
     kfn = "moe_gemm_small_kernel" if B <= 32 else "moe_gemm_kernel"  # register-fed below 64-token blocks
-    kname = f"{kfn}<{wl.fmt},{'gated' if dom == 'gemm1' else 'plain'},BN={B}>"
+    stage = ("gated" if wl.gated else "relu2") if dom == "gemm1" else "plain"
+    kname = f"{kfn}<{wl.fmt},{stage},BN={B}>"
     if tensor_bound:
         achieved = alg[f"flops_{dom}"] / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_burst, "unit": "TFLOP/s",

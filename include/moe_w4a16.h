@@ -62,11 +62,15 @@ typedef enum moe_status {
  *              scale per expert (the same for gate and up rows). */
 typedef enum moe_wfmt { MOE_W_INT4_U4B8 = 0, MOE_W_MXFP4 = 1, MOE_W_NVFP4 = 2 } moe_wfmt;
 
-/* Gated activations; gate = first N outputs of GEMM1, up = the next N.
+/* Activations.  Gated experts: gate = first N outputs of GEMM1, up = the next N.
  *   SILU_MUL:      silu(gate) * up                         (silu_and_mul)
  *   SIGMOID_ALPHA: g = min(gate, limit), u = clamp(up, -limit, limit),
- *                  g * sigmoid(alpha * g) * (u + 1)         (GPT-OSS) */
-typedef enum moe_act { MOE_ACT_SILU_MUL = 0, MOE_ACT_SIGMOID_ALPHA = 1 } moe_act;
+ *                  g * sigmoid(alpha * g) * (u + 1)         (GPT-OSS)
+ * Non-gated experts (moe_layer_desc.non_gated = 1): GEMM1 has N outputs h.
+ *   RELU2:         relu(h)^2   (activation="relu2", is_gated=False of the
+ *                  large-M schedule test in "Marlin MoE kernel occupancy ...",
+ *                  sglang PR #31552) */
+typedef enum moe_act { MOE_ACT_SILU_MUL = 0, MOE_ACT_SIGMOID_ALPHA = 1, MOE_ACT_RELU2 = 2 } moe_act;
 
 /* Shape of one layer's expert bank held by this GPU. */
 typedef struct moe_layer_desc {
@@ -79,6 +83,8 @@ typedef struct moe_layer_desc {
     int32_t w13_interleaved;  /* 1: w13 rows stored gate0, up0, gate1, up1, ... (GPT-OSS) */
     int32_t has_bias13;       /* 1: per-expert bf16 bias on GEMM1 outputs */
     int32_t has_bias2;        /* 1: per-expert bf16 bias on GEMM2 outputs */
+    int32_t non_gated;        /* 0: w13 holds gate and up rows (2N); 1: w13 holds N rows and
+                                 the activation is MOE_ACT_RELU2 (w13_interleaved must be 0) */
 } moe_layer_desc;
 
 /* ------------------------------------------------------------------ repack
@@ -88,15 +94,17 @@ typedef struct moe_layer_desc {
  * opaque blob of moe_repack_size() bytes that moe_w4a16_forward reads.
  *
  * Inputs (device pointers):
- *   w13    uint8 [E, 2N, K/2]   packed codes (gate rows then up rows, or interleaved)
- *   w13_s  [E, 2N, K/g]         bf16 (INT4) | uint8 E8M0 (MXFP4) | uint8 E4M3 (NVFP4)
+ *   w13    uint8 [E, R, K/2]    packed codes; R = 2N gated (gate rows then up rows, or
+ *                               interleaved), R = N non-gated
+ *   w13_s  [E, R, K/g]          bf16 (INT4) | uint8 E8M0 (MXFP4) | uint8 E4M3 (NVFP4)
  *   w13_gs fp32 [E]             NVFP4 only, else NULL
- *   b13    bf16 [E, 2N]         when has_bias13, else NULL (same row order as w13)
+ *   b13    bf16 [E, R]          when has_bias13, else NULL (same row order as w13)
  *   w2     uint8 [E, K, N/2];  w2_s [E, K, N/g];  w2_gs fp32 [E] (NVFP4);
  *   b2     bf16 [E, K]          when has_bias2, else NULL
  *   packed device buffer of moe_repack_size() bytes, 256-byte aligned.
- * Returns MOE_ERR_INVALID for shapes outside the rules above or odd 2N rows
- * when interleaved (the ValueError cases of deinterleave_moe_mxfp4_w13_for_marlin). */
+ * Returns MOE_ERR_INVALID for shapes outside the rules above, odd 2N rows
+ * when interleaved (the ValueError cases of deinterleave_moe_mxfp4_w13_for_marlin)
+ * or non_gated together with w13_interleaved. */
 int64_t moe_repack_size(const moe_layer_desc* desc);
 int moe_repack_weights(const moe_layer_desc* desc, const void* w13, const void* w13_s,
                        const float* w13_gs, const void* b13, const void* w2, const void* w2_s,
@@ -137,8 +145,8 @@ int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int blo
 /* The layer ("013-moe-middle-tiles.py" kernel_fn after alignment; PR #31552
  * fused_marlin_moe and the per-expert reference loop of its large-M test):
  *   for every local pair p = (t, j) with expert e:
- *     h = gs13[e] * x[t] . W13[e]^T + b13[e]                  [2N]
- *     a = act(h[:N], h[N:])                                    [N]
+ *     h = gs13[e] * x[t] . W13[e]^T + b13[e]                  [2N] ([N] non-gated)
+ *     a = act(h[:N], h[N:])   (relu(h)^2 non-gated)            [N]
  *     y = gs2[e] * a . W2[e]^T + b2[e]                         [K]
  *   out[t] = bf16(rsf * sum_j topk_weights[t,j] * y_(t,j))      (post_norm_w == NULL)
  *   out[t] = bf16(rsf * sum_j topk_weights[t,j] * inv_j * z_j),  z = y * nw,
@@ -151,7 +159,8 @@ int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int blo
  * Arguments (device unless said): packed from moe_repack_weights for `desc`;
  * x bf16 [M, K]; topk_ids int32 [M, top_k]; topk_weights fp32 [M, top_k];
  * sorted_ids / expert_ids / n_padded from moe_align with the same M, top_k,
- * expert_base, E and block_m; act a moe_act; alpha, limit (host) for
+ * expert_base, E and block_m; act a moe_act (MOE_ACT_RELU2 exactly when
+ * desc->non_gated); alpha, limit (host) for
  * SIGMOID_ALPHA (limit = +inf: no clamp); post_norm_w bf16 [K] or NULL;
  * out bf16 [M, K]; workspace of at least moe_workspace_size() bytes.  packed and
  * workspace must be 256-byte aligned; x, out and post_norm_w 16-byte aligned.

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from weight_only_bit_moe_gb300 import workloads as wk
-from gpu_util import GPU_SMALL, bf16_to_f32, check_close, need_gpu, run_layer, sample_tokens
+from gpu_util import GPU_SMALL, bf16_to_f32, check_close, check_workload, need_gpu, run_layer, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -87,19 +87,20 @@ def test_forward_small(name):
     layer = _layer(W)
     out = run_layer(layer, wl, X)
     ref = bf16_to_f32(oracle.forward_workload(wl, W, X))
-    check_close(out.float().cpu().numpy(), ref, name)
+    check_workload(out.float().cpu().numpy(), ref, wl, name)
     assert layer.status() == 0
 
 
+@pytest.mark.parametrize("name", ["int4-zipf-small", "int4-relu2-small"])
 @pytest.mark.parametrize("B", [8, 16, 32, 64, 128])
-def test_forward_every_block_m(B):
-    wl = GPU_SMALL["int4-zipf-small"]
+def test_forward_every_block_m(name, B):
+    wl = GPU_SMALL[name]
     W = wk.make_weights(wl, 41)
     X = wk.make_batch(wl, 50, 42)
     layer = _layer(W)
     out = run_layer(layer, wl, X, block_m=B)
     ref = bf16_to_f32(oracle.forward_workload(wl, W, X))
-    check_close(out.float().cpu().numpy(), ref, f"block_m={B}")
+    check_workload(out.float().cpu().numpy(), ref, wl, f"{name} block_m={B}")
 
 
 def test_forward_bitwise_reproducible():
@@ -146,7 +147,7 @@ def test_forward_single_token():
 FULL = [("tiny-int4", 16), ("int4-bias", 123), ("int4-bias", 2304), ("mxfp4-alpha", 1), ("mxfp4-alpha", 32),
         ("mxfp4-alpha", 1024), ("nvfp4-ep-norm", 1), ("nvfp4-ep-norm", 8), ("nvfp4-ep-norm", 64),
         ("nvfp4-ep-norm", 512), ("int4-skew", 1), ("int4-skew", 16), ("int4-skew", 256), ("int4-skew", 4096),
-        ("int4-uniform", 16), ("int4-uniform", 4096)]
+        ("int4-uniform", 16), ("int4-uniform", 4096), ("int4-relu2", 123), ("int4-relu2", 2304)]
 
 _weights_cache = {}
 
@@ -167,7 +168,7 @@ def test_forward_full_sampled(name, M):
     out = run_layer(layer, wl, X)
     toks = sample_tokens(M, 12 if wl.K * wl.N > 4096 * 1536 else 16, seed=M)
     ref = bf16_to_f32(oracle.forward_workload(wl, W, X, tokens=toks))
-    check_close(out.float().cpu().numpy()[toks], ref, f"{name} M={M}")
+    check_workload(out.float().cpu().numpy()[toks], ref, wl, f"{name} M={M}")
     assert layer.status() == 0
 
 

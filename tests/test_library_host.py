@@ -52,6 +52,22 @@ def test_repack_size_rules(lib):
             lib.moe_repack_size(bad)
 
 
+def test_non_gated_layout_rules(lib):
+    """Non-gated w13 tiles hold 256 rows of h instead of 128 gate + 128 up rows:
+    at K=512, N=1024 (INT4, 8 experts) the bank loses half its w13 tiles -- 4
+    tiles x 4 scale periods x (512 scale bytes + 2 x 8192 code bytes) per expert --
+    and half its GEMM1 bias (1024 bf16 per expert)."""
+    D = lib.moe_layer_desc
+    gated = lib.moe_repack_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 0))
+    plain = lib.moe_repack_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 1))
+    assert gated - plain == 8 * 4 * 4 * (512 + 2 * 8192) + 8 * 1024 * 2
+    assert lib.moe_repack_size(D(1, 4, 192, 160, 32, 0, 0, 0, 1)) > 0   # N pads to 256
+    for bad in [D(1, 8, 512, 512, 32, 1, 0, 0, 1),    # non-gated rows cannot be interleaved
+                D(0, 8, 512, 1024, 128, 0, 0, 0, 2)]:  # flag is 0 or 1
+        with pytest.raises(lib.MoeError):
+            lib.moe_repack_size(bad)
+
+
 def test_rejects_bad_arguments_without_device(lib):
     L = lib.load()
     # align: bad block_m, too many experts, null outputs -> MOE_ERR_INVALID before any CUDA call
@@ -77,6 +93,16 @@ def test_rejects_bad_arguments_without_device(lib):
     zero = list(args)
     zero[3] = 0          # M == 0 is a no-op
     assert fwd(*zero) == lib.MOE_OK
+    # the activation must match the experts' gating, even for an empty batch
+    relu2_on_gated = list(zero)
+    relu2_on_gated[12] = lib.MOE_ACT_RELU2
+    assert fwd(*relu2_on_gated) == lib.MOE_ERR_INVALID
+    ng = lib.moe_layer_desc(0, 8, 512, 1024, 128, 0, 0, 0, 1)
+    silu_on_plain = list(zero)
+    silu_on_plain[0] = ctypes.byref(ng)
+    assert fwd(*silu_on_plain) == lib.MOE_ERR_INVALID
+    silu_on_plain[12] = lib.MOE_ACT_RELU2
+    assert fwd(*silu_on_plain) == lib.MOE_OK
     assert lib.status_string(lib.MOE_ERR_TIMEOUT) == "device wait timed out"
 
 

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "_build", f"libmoe_w4a16_{platform.machine()}.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 MOE_W_INT4_U4B8, MOE_W_MXFP4, MOE_W_NVFP4 = 0, 1, 2
-MOE_ACT_SILU_MUL, MOE_ACT_SIGMOID_ALPHA = 0, 1
+MOE_ACT_SILU_MUL, MOE_ACT_SIGMOID_ALPHA, MOE_ACT_RELU2 = 0, 1, 2
 
 EXPORTED = ("moe_repack_size", "moe_repack_weights", "moe_align_capacity", "moe_align", "moe_choose_block_m",
             "moe_workspace_size", "moe_w4a16_forward", "moe_w4a16_forward_noalloc", "moe_get_status",
@@ -34,7 +34,7 @@ class MoeError(RuntimeError):
 class moe_layer_desc(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("inter", ctypes.c_int32), ("group_size", ctypes.c_int32), ("w13_interleaved", ctypes.c_int32),
-                ("has_bias13", ctypes.c_int32), ("has_bias2", ctypes.c_int32)]
+                ("has_bias13", ctypes.c_int32), ("has_bias2", ctypes.c_int32), ("non_gated", ctypes.c_int32)]
 
 
 _lib = None

@@ -52,7 +52,8 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   // split-K only runs while tiles * blocks < grid, so the partial rows stay below this bound
   w->rows1 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T1 + 1) * block_m);
   w->rows2 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T2 + 1) * block_m);
-  const int64_t per1 = (int64_t)w->rows1 * 2 * L.Npad * 4, per2 = (int64_t)w->rows2 * L.K * 4;
+  // fp32 partial rows: GEMM1 gate and up (or h alone), GEMM2 the output width
+  const int64_t per1 = (int64_t)w->rows1 * (L.gated ? 2 : 1) * L.Npad * 4, per2 = (int64_t)w->rows2 * L.K * 4;
   w->max_split1 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per1 ? split_budget / per1 : 1));
   w->max_split2 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per2 ? split_budget / per2 : 1));
   int64_t off = 0;
@@ -78,11 +79,11 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   return true;
 }
 
-cudaError_t launch_gemm(int fmt, bool small, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
+cudaError_t launch_gemm(int fmt, bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
   switch (fmt) {
-    case MOE_W_INT4_U4B8: return launch_gemm_int4(small, gated, bn, g, grid, st);
-    case MOE_W_MXFP4: return launch_gemm_mxfp4(small, gated, bn, g, grid, st);
-    case MOE_W_NVFP4: return launch_gemm_nvfp4(small, gated, bn, g, grid, st);
+    case MOE_W_INT4_U4B8: return launch_gemm_int4(small, stage, bn, g, grid, st);
+    case MOE_W_MXFP4: return launch_gemm_mxfp4(small, stage, bn, g, grid, st);
+    case MOE_W_NVFP4: return launch_gemm_nvfp4(small, stage, bn, g, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -163,7 +164,9 @@ static int check_forward_args(const moe_layer_desc* desc, const void* packed, co
                               const void* post_norm_w, const void* out, Layout* L) {
   if (!desc || !make_layout(*desc, L)) return MOE_ERR_INVALID;
   if (M < 0 || top_k <= 0 || top_k > 16 || !valid_block_m(block_m)) return MOE_ERR_INVALID;
-  if (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SIGMOID_ALPHA) return MOE_ERR_INVALID;
+  // gated experts take a gated activation, non-gated ones relu^2
+  if (L->gated ? (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SIGMOID_ALPHA) : act != MOE_ACT_RELU2)
+    return MOE_ERR_INVALID;
   if ((int64_t)M * top_k >= (int64_t)1 << 31) return MOE_ERR_INVALID;
   if (M == 0) return MOE_OK;
   if (!packed || !x || !topk_ids || !topk_weights || !sorted_ids || !expert_ids || !n_padded || !out)
@@ -230,7 +233,8 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.split_rows = w.rows1;
   g.partial = reinterpret_cast<float*>(ws + w.part1_off);
   g.counters = reinterpret_cast<int32_t*>(ws + w.counters1_off);
-  if (launch_gemm(L.fmt, small, true, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(L.fmt, small, L.gated ? kGemm1Gated : kGemm1Relu2, bn, g, w.grid, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (trace(1, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   // GEMM2
@@ -240,7 +244,7 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.split_rows = w.rows2;
   g.partial = reinterpret_cast<float*>(ws + w.part2_off);
   g.counters = reinterpret_cast<int32_t*>(ws + w.counters2_off);
-  if (launch_gemm(L.fmt, small, false, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(L.fmt, small, kGemm2, bn, g, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(2, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   // combine

@@ -18,9 +18,12 @@ namespace moe {
 // operands ("halves").  GEMM1 tile i holds gate rows [128i, 128i+128) in half 0
 // and the matching up rows in half 1, so one TMEM lane holds the gate and up
 // value of the same intermediate feature and the activation runs in the GEMM1
-// epilogue.  GEMM2 tile i holds output rows [256i, 256i+256).  N is zero-padded
-// to Npad = roundup(N, 128) and GEMM2's rows to roundup(K, 256) (the pages'
-// _pad_w13/_pad_w2 tile padding); padded codes decode to 0.
+// epilogue.  Non-gated experts (relu(h)^2) have no up rows: their GEMM1 tile i
+// holds rows [256i, 256i+256) of h, like GEMM2.  GEMM2 tile i holds output
+// rows [256i, 256i+256).  N is zero-padded to Npad = roundup(N, 128) (gated)
+// or roundup(N, 256) (non-gated), GEMM2's rows to roundup(K, 256) (the pages'
+// _pad_w13/_pad_w2 tile padding); padded codes decode to 0 and padded bias
+// entries are 0, so padded features of a are 0 under every activation.
 //
 // Each tile is a sequence of K-stages of 64 reduction elements.  A stage's
 // packed codes are 8 KiB: uint4 units [j][r] (j = 0,1, r the tile row), so
@@ -44,11 +47,19 @@ constexpr int kTileRows = 256;       // weight rows per CTA tile (2 x 128)
 constexpr int kStageK = 64;          // reduction elements per stage
 constexpr int kPackedStageBytes = kTileRows * kStageK / 2;  // 8192
 
+// Which matmul a GEMM kernel instance computes.
+enum GemmStage : int {
+  kGemm2 = 0,       // y = gs2 * a . W2^T + b2, fp32 rows by pair
+  kGemm1Gated = 1,  // a = act(gate, up) of h = gs13 * x . W13^T + b13, fp16
+  kGemm1Relu2 = 2,  // a = relu(h)^2, non-gated experts, fp16
+};
+
 struct Layout {
   int fmt, E, K, N, group;
-  int Npad;        // roundup(N, 128)
+  int gated;       // 1: GEMM1 tiles pair 128 gate rows with their 128 up rows; 0: 256 rows of h
+  int Npad;        // roundup(N, 128) gated, roundup(N, 256) non-gated
   int Kpad2;       // roundup(K, 256)
-  int T1, T2;      // GEMM1 tiles (Npad/128), GEMM2 tiles (Kpad2/256)
+  int T1, T2;      // GEMM1 tiles (Npad/128 or Npad/256), GEMM2 tiles (Kpad2/256)
   int S1, S2;      // stages per tile: K/64 and Npad/64
   int period;      // stages per scale chunk: 2 (INT4) or 1
   int scale_bytes; // scale bytes per chunk
@@ -65,14 +76,17 @@ __host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
   if (d.group_size != want_group) return false;
   if (d.hidden % 64 || d.inter % d.group_size) return false;
   if (d.fmt == MOE_W_INT4_U4B8 && d.hidden % 128) return false;
+  if (d.non_gated != 0 && (d.non_gated != 1 || d.w13_interleaved)) return false;
   L->fmt = d.fmt;
   L->E = d.num_experts;
   L->K = d.hidden;
   L->N = d.inter;
   L->group = d.group_size;
-  L->Npad = (int)round_up64(d.inter, 128);
+  L->gated = d.non_gated ? 0 : 1;
+  const int f1 = L->gated ? 128 : 256;  // intermediate features per GEMM1 tile
+  L->Npad = (int)round_up64(d.inter, f1);
   L->Kpad2 = (int)round_up64(d.hidden, 256);
-  L->T1 = L->Npad / 128;
+  L->T1 = L->Npad / f1;
   L->T2 = L->Kpad2 / 256;
   L->S1 = d.hidden / kStageK;
   L->S2 = L->Npad / kStageK;
@@ -87,7 +101,7 @@ __host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
   L->w2_off = off = round_up64(off, 256);
   off += (int64_t)L->E * L->T2 * L->tile2_bytes;
   L->b13_off = off = round_up64(off, 256);
-  if (d.has_bias13) off += (int64_t)L->E * 2 * L->Npad * 2;
+  if (d.has_bias13) off += (int64_t)L->E * (L->gated ? 2 : 1) * L->Npad * 2;
   L->b2_off = off = round_up64(off, 256);
   if (d.has_bias2) off += (int64_t)L->E * L->Kpad2 * 2;
   L->gs13_off = off = round_up64(off, 256);

@@ -1,5 +1,5 @@
 // Grouped W4A16 GEMM on tcgen05 tensor cores (sm_103a), shared by GEMM1 (w13,
-// fused gated activation) and GEMM2 (w2).
+// fused gated or relu^2 activation) and GEMM2 (w2).
 //
 // The function is Marlin's moe_wna16_marlin_gemm as called twice by
 // "013-moe-middle-tiles.py" kernel_fn (GEMM1 with top_k = 8 over x, GEMM2 with
@@ -33,8 +33,9 @@
 //     reproducible, no spinning);
 //   * one elected lane of the MMA warp issues tcgen05.mma into TMEM accumulators (double-buffered up
 //     to 64 tokens); eight epilogue warps (two per TMEM lane quarter, splitting
-//     the token columns) add bias and scales, apply the activation (GEMM1) or
-//     write rows to their pairs (GEMM2).
+//     the token columns) add bias and scales, apply the activation (GEMM1:
+//     act(gate, up) of a lane's two halves, or relu(h)^2 of each half for
+//     non-gated experts) or write rows to their pairs (GEMM2).
 #pragma once
 
 #include <cuda.h>
@@ -118,6 +119,8 @@ __device__ __forceinline__ float act_fn(int kind, float g, float u, float alpha,
   const float hg = 0.5f * gc;
   return fmaf(hg, tanh_approx(alpha * hg), hg) * (uc + 1.0f);  // gc * sigmoid(alpha * gc) * (uc + 1)
 }
+// Activation of non-gated experts: relu(h)^2.
+__device__ __forceinline__ float relu2(float h) { return h > 0.0f ? h * h : 0.0f; }
 
 struct WorkPlan {
   int nb;      // valid blocks
@@ -179,8 +182,10 @@ __device__ __forceinline__ void tma_tile3d(uint32_t dst, const CUtensorMap* map,
       : "memory");
 }
 
-template <int FMT, bool GATED, int BN>
+template <int FMT, int STAGE, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
+  constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
+  constexpr bool kGated = STAGE == kGemm1Gated;  // tile halves are gate and up rows
   using SM = GemmSmem<BN>;
   using PF = PackedFmt<FMT>;
   constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc;
@@ -233,9 +238,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   // read the predecessor's rows or write counters and outputs, wait first.
   grid_dependents_launch();
 
-  const WorkPlan plan = make_plan(g, GATED);
-  const int64_t tile_bytes = GATED ? L.tile1_bytes : L.tile2_bytes;
-  const uint8_t* wbase = g.packed + (GATED ? L.w13_off : L.w2_off);
+  const WorkPlan plan = make_plan(g, kG1);
+  const int64_t tile_bytes = kG1 ? L.tile1_bytes : L.tile2_bytes;
+  const uint8_t* wbase = g.packed + (kG1 ? L.w13_off : L.w2_off);
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer (packed weights)
@@ -430,10 +435,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     const int hr = q * 32 + lane;      // row within each 128-row half
     const int et = threadIdx.x - kWarpEpi0 * 32;  // 0..255
     const int csub = (warp - kWarpEpi0) >> 2;      // which 8-column chunks this warp takes
-    const float* gs_tab = reinterpret_cast<const float*>(g.packed + (GATED ? L.gs13_off : L.gs2_off));
-    const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (GATED ? L.b13_off : L.b2_off));
+    const float* gs_tab = reinterpret_cast<const float*>(g.packed + (kG1 ? L.gs13_off : L.gs2_off));
+    const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (kG1 ? L.b13_off : L.b2_off));
     const int Npad = L.Npad;
-    const int width = GATED ? 2 * Npad : L.K;  // partial row width
+    const int width = kGated ? 2 * Npad : (kG1 ? Npad : L.K);  // partial row width
+    const int bias_stride = kGated ? 2 * Npad : (kG1 ? Npad : L.Kpad2);
     uint32_t ic = 0;
     for (int w = blockIdx.x; w < plan.items; w += gridDim.x, ++ic) {
       int b, tile, split;
@@ -446,21 +452,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       const int e = g.expert_ids[b];
       const float gsc = gs_tab[e];
       // feature / output rows held by this thread in half 0 and half 1; for
-      // GEMM1 both halves hold the same feature (gate and up)
-      int row0, row1, col0, col1;  // col*: index in the partial row
-      if (GATED) { row0 = tile * 128 + hr; row1 = row0; col0 = row0; col1 = Npad + row0; }
+      // gated GEMM1 both halves hold the same feature (gate and up)
+      int row0, row1, col0, col1;  // col*: index in the partial row and in the bias row
+      if (kGated) { row0 = tile * 128 + hr; row1 = row0; col0 = row0; col1 = Npad + row0; }
       else { row0 = tile * 256 + hr; row1 = row0 + 128; col0 = row0; col1 = row1; }
       float bias0 = 0.f, bias1 = 0.f;
       if (g.has_bias) {
-        if (GATED) {
-          bias0 = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + row0]);
-          bias1 = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + Npad + row1]);
-        } else {
-          bias0 = bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + row0]);
-          bias1 = bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + row1]);
-        }
+        bias0 = bf16_bits_to_float(bias_tab[(int64_t)e * bias_stride + col0]);
+        bias1 = bf16_bits_to_float(bias_tab[(int64_t)e * bias_stride + col1]);
       }
-      const bool ok0 = GATED || row0 < L.K, ok1 = GATED || row1 < L.K;
+      const bool ok0 = kG1 || row0 < L.K, ok1 = kG1 || row1 < L.K;
       named_bar_sync(2, kEpiThreads);
       const int accb = ic % kNacc;
       mbar_wait(&acc_full[accb], (ic / kNacc) & 1, abort_flag, g.status);
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           const uint4 sa = lds128(epi_sid_s + 4 * c0), sb = lds128(epi_sid_s + 4 * c0 + 16);
           const int sid[8] = {(int)sa.x, (int)sa.y, (int)sa.z, (int)sa.w, (int)sb.x, (int)sb.y, (int)sb.z, (int)sb.w};
           const int pos0 = b * g.block_m + c0;
-          if (GATED) {
+          if (kGated) {
             float av[8];
             if (g.act_kind == MOE_ACT_SILU_MUL) {
 #pragma unroll
@@ -553,6 +554,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             for (int jj = 0; jj < 8; ++jj)
               if (c0 + jj < jmax)
                 g.a_out[(int64_t)(pos0 + jj) * Npad + row0] = __half_as_ushort(__float2half_rn(sid[jj] < g.pairs ? av[jj] : 0.0f));
+          } else if (kG1) {  // non-gated: both halves are features, a = relu(h)^2
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+              if (c0 + jj < jmax) {
+                const bool live = sid[jj] < g.pairs;
+                const float a0 = live ? relu2(f0[jj] * gsc + bias0) : 0.0f;
+                const float a1 = live ? relu2(f1[jj] * gsc + bias1) : 0.0f;
+                uint16_t* dst = g.a_out + (int64_t)(pos0 + jj) * Npad;
+                dst[row0] = __half_as_ushort(__float2half_rn(a0));
+                dst[row1] = __half_as_ushort(__float2half_rn(a1));
+              }
           } else {
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj)

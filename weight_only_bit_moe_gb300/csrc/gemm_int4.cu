@@ -2,7 +2,7 @@
 #include "gemm_launch.cuh"
 
 namespace moe {
-cudaError_t launch_gemm_int4(bool small, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
-  return small ? launch_gemm_small_fmt<MOE_W_INT4_U4B8>(gated, bn, g, grid, st) : launch_gemm_fmt<MOE_W_INT4_U4B8>(gated, bn, g, grid, st);
+cudaError_t launch_gemm_int4(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
+  return small ? launch_gemm_small_fmt<MOE_W_INT4_U4B8>(stage, bn, g, grid, st) : launch_gemm_fmt<MOE_W_INT4_U4B8>(stage, bn, g, grid, st);
 }
 }  // namespace moe

@@ -7,9 +7,9 @@
 
 namespace moe {
 
-// Launch one (FMT, GATED, BN) instance on `grid` CTAs; sets the kernel's
+// Launch one (FMT, STAGE, BN) instance on `grid` CTAs; sets the kernel's
 // dynamic shared-memory limit once per device.
-template <int FMT, bool GATED, int BN>
+template <int FMT, int STAGE, int BN>
 cudaError_t launch_gemm_instance(const GemmArgs& g, int grid, cudaStream_t st) {
   static bool configured[64] = {};
   int dev = 0;
@@ -17,25 +17,35 @@ cudaError_t launch_gemm_instance(const GemmArgs& g, int grid, cudaStream_t st) {
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<FMT, GATED, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(moe_gemm_kernel<FMT, STAGE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                GemmSmem<BN>::kAlloc);
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
-  return launch_dependent(moe_gemm_kernel<FMT, GATED, BN>, dim3(grid), dim3(kGemmThreads), GemmSmem<BN>::kAlloc, st, g);
+  return launch_dependent(moe_gemm_kernel<FMT, STAGE, BN>, dim3(grid), dim3(kGemmThreads), GemmSmem<BN>::kAlloc, st, g);
+}
+
+template <int FMT, int BN>
+cudaError_t launch_gemm_stage(int stage, const GemmArgs& g, int grid, cudaStream_t st) {
+  switch (stage) {
+    case kGemm2: return launch_gemm_instance<FMT, kGemm2, BN>(g, grid, st);
+    case kGemm1Gated: return launch_gemm_instance<FMT, kGemm1Gated, BN>(g, grid, st);
+    case kGemm1Relu2: return launch_gemm_instance<FMT, kGemm1Relu2, BN>(g, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int FMT>
-cudaError_t launch_gemm_fmt(bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
+cudaError_t launch_gemm_fmt(int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
   switch (bn) {
-    case 64: return gated ? launch_gemm_instance<FMT, true, 64>(g, grid, st) : launch_gemm_instance<FMT, false, 64>(g, grid, st);
-    case 128: return gated ? launch_gemm_instance<FMT, true, 128>(g, grid, st) : launch_gemm_instance<FMT, false, 128>(g, grid, st);
+    case 64: return launch_gemm_stage<FMT, 64>(stage, g, grid, st);
+    case 128: return launch_gemm_stage<FMT, 128>(stage, g, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 // Register-fed kernel for token blocks of 8, 16 or 32 (gemm_small.cuh).
-template <int FMT, bool GATED, int BN>
+template <int FMT, int STAGE, int BN>
 cudaError_t launch_gemm_small_instance(const GemmArgs& g, int grid, cudaStream_t st) {
   static bool configured[64] = {};
   int dev = 0;
@@ -43,28 +53,39 @@ cudaError_t launch_gemm_small_instance(const GemmArgs& g, int grid, cudaStream_t
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    err = cudaFuncSetAttribute(moe_gemm_small_kernel<FMT, GATED, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(moe_gemm_small_kernel<FMT, STAGE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SmallSmem<BN>::kAlloc);
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
-  return launch_dependent(moe_gemm_small_kernel<FMT, GATED, BN>, dim3(grid), dim3(kSmallThreads),
+  return launch_dependent(moe_gemm_small_kernel<FMT, STAGE, BN>, dim3(grid), dim3(kSmallThreads),
                           SmallSmem<BN>::kAlloc, st, g);
 }
 
-template <int FMT>
-cudaError_t launch_gemm_small_fmt(bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
-  switch (bn) {
-    case 8: return gated ? launch_gemm_small_instance<FMT, true, 8>(g, grid, st) : launch_gemm_small_instance<FMT, false, 8>(g, grid, st);
-    case 16: return gated ? launch_gemm_small_instance<FMT, true, 16>(g, grid, st) : launch_gemm_small_instance<FMT, false, 16>(g, grid, st);
-    case 32: return gated ? launch_gemm_small_instance<FMT, true, 32>(g, grid, st) : launch_gemm_small_instance<FMT, false, 32>(g, grid, st);
+template <int FMT, int BN>
+cudaError_t launch_gemm_small_stage(int stage, const GemmArgs& g, int grid, cudaStream_t st) {
+  switch (stage) {
+    case kGemm2: return launch_gemm_small_instance<FMT, kGemm2, BN>(g, grid, st);
+    case kGemm1Gated: return launch_gemm_small_instance<FMT, kGemm1Gated, BN>(g, grid, st);
+    case kGemm1Relu2: return launch_gemm_small_instance<FMT, kGemm1Relu2, BN>(g, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-// small = true selects the register-fed kernel (bn = block_m in {8, 16, 32}).
-cudaError_t launch_gemm_int4(bool small, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st);
-cudaError_t launch_gemm_mxfp4(bool small, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st);
-cudaError_t launch_gemm_nvfp4(bool small, bool gated, int bn, const GemmArgs& g, int grid, cudaStream_t st);
+template <int FMT>
+cudaError_t launch_gemm_small_fmt(int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st) {
+  switch (bn) {
+    case 8: return launch_gemm_small_stage<FMT, 8>(stage, g, grid, st);
+    case 16: return launch_gemm_small_stage<FMT, 16>(stage, g, grid, st);
+    case 32: return launch_gemm_small_stage<FMT, 32>(stage, g, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// small = true selects the register-fed kernel (bn = block_m in {8, 16, 32});
+// stage is a GemmStage.
+cudaError_t launch_gemm_int4(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st);
+cudaError_t launch_gemm_mxfp4(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st);
+cudaError_t launch_gemm_nvfp4(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st);
 
 }  // namespace moe

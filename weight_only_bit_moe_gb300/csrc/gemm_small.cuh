@@ -4,8 +4,8 @@
 // bandwidth, not by tensor math.
 //
 // Same function as moe_gemm_kernel (gemm.cuh) -- GEMM1 with the fused gated
-// activation, or GEMM2 -- on the same packed layout, built for a different
-// bottleneck:
+// or relu^2 activation, or GEMM2 -- on the same packed layout, built for a
+// different bottleneck:
 //
 //   * weights reach registers, never tensor memory: eight consumer warps each
 //     own 32 rows of the 256-row tile, load their 4-bit codes from the staged
@@ -15,9 +15,10 @@
 //     8-wide N side.  At 8..32 tokens a 64-K stage costs 128..512 tensor
 //     cycles per SM, under the ~380 cycles HBM needs to deliver it, and no
 //     cross-warp handoff sits between dequantisation and the MMA;
-//   * GEMM1 pairs gate and up rows inside each 16-row fragment (rows 0..7 gate
-//     features, rows 8..15 the same up features), so the activation is applied
-//     in the registers that hold both accumulators;
+//   * gated GEMM1 pairs gate and up rows inside each 16-row fragment (rows
+//     0..7 gate features, rows 8..15 the same up features), so the activation
+//     is applied in the registers that hold both accumulators; non-gated GEMM1
+//     and GEMM2 take 16 consecutive rows per fragment;
 //   * one producer thread streams 4-stage chunks (~34 KB of packed codes and
 //     scales in one bulk copy, plus the block's activation rows for those
 //     stages in one 3-D TMA tile) into a 4..6-deep ring; large copies keep a
@@ -235,8 +236,10 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
   }
 }
 
-template <int FMT, bool GATED, int BN>
+template <int FMT, int STAGE, int BN>
 __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const __grid_constant__ GemmArgs g) {
+  constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
+  constexpr bool kGated = STAGE == kGemm1Gated;  // fragment rows pair gate and up features
   using SM = SmallSmem<BN>;
   constexpr int kSlots = SM::kSlots;
   constexpr int NT = BN / 8;  // 8-token column tiles
@@ -268,9 +271,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
   // predecessor: every thread that touches them waits first.
   grid_dependents_launch();
 
-  const WorkPlan plan = make_plan_small(g, GATED, BN);
-  const int64_t tile_bytes = GATED ? L.tile1_bytes : L.tile2_bytes;
-  const uint8_t* wbase = g.packed + (GATED ? L.w13_off : L.w2_off);
+  const WorkPlan plan = make_plan_small(g, kG1, BN);
+  const int64_t tile_bytes = kG1 ? L.tile1_bytes : L.tile2_bytes;
+  const uint8_t* wbase = g.packed + (kG1 ? L.w13_off : L.w2_off);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     int (&rows)[kSmallMI][2] = F.rows;
 #pragma unroll
     for (int i = 0; i < kSmallMI; ++i) {
-      if (GATED) {  // gate feature f in fragment row gq, its up row in gq + 8
+      if (kGated) {  // gate feature f in fragment row gq, its up row in gq + 8
         rows[i][0] = 8 * (kSmallMI * cw + i) + gq;
         rows[i][1] = 128 + rows[i][0];
       } else {
@@ -368,10 +371,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         for (int j = 0; j < 4; ++j) F.b_off[j][q] = n * 128 + ((((uint32_t)(2 * j) + sel) ^ (n & 7)) << 4);
       }
     }
-    const float* gs_tab = reinterpret_cast<const float*>(g.packed + (GATED ? L.gs13_off : L.gs2_off));
-    const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (GATED ? L.b13_off : L.b2_off));
+    const float* gs_tab = reinterpret_cast<const float*>(g.packed + (kG1 ? L.gs13_off : L.gs2_off));
+    const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (kG1 ? L.b13_off : L.b2_off));
     const int Npad = L.Npad;
-    const int width = GATED ? 2 * Npad : L.K;
+    const int width = kGated ? 2 * Npad : (kG1 ? Npad : L.K);  // partial row width
+    const int out_rows = kG1 ? Npad : L.K;                     // rows of the tile that exist
     uint32_t m[kSmallMI][2][4] = {};
     uint32_t ck = 0;
 
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
             for (int c = 0; c < 2; ++c) {
               const int pos = b * g.block_m + n * 8 + 2 * tq + c;
               float* dst = g.partial + ((int64_t)split * g.split_rows + pos) * width;
-              if (GATED) {
+              if (kGated) {
                 const int f = tile * 128 + rows[i][0];
                 __stcg(dst + f, acc[i][n][c]);
                 __stcg(dst + Npad + f, acc[i][n][2 + c]);
@@ -423,7 +427,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int o = tile * 256 + rows[i][h];
-                  if (o < L.K) __stcg(dst + o, acc[i][n][2 * h + c]);
+                  if (o < out_rows) __stcg(dst + o, acc[i][n][2 * h + c]);
                 }
               }
             }
@@ -456,7 +460,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
               for (int c = 0; c < 2; ++c) {
                 const int pos = b * g.block_m + n * 8 + 2 * tq + c;
                 const float* src = g.partial + ((int64_t)sp * g.split_rows + pos) * width;
-                if (GATED) {
+                if (kGated) {
                   const int f = tile * 128 + rows[i][0];
                   acc[i][n][c] += __ldcg(src + f);
                   acc[i][n][2 + c] += __ldcg(src + Npad + f);
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
 #pragma unroll
                   for (int h = 0; h < 2; ++h) {
                     const int o = tile * 256 + rows[i][h];
-                    if (o < L.K) acc[i][n][2 * h + c] += __ldcg(src + o);
+                    if (o < out_rows) acc[i][n][2 * h + c] += __ldcg(src + o);
                   }
                 }
               }
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       const float gsc = gs_tab[e];
 #pragma unroll
       for (int i = 0; i < kSmallMI; ++i) {
-        if (GATED) {
+        if (kGated) {
           const int f = tile * 128 + rows[i][0];
           float bg = 0.f, bu = 0.f;
           if (g.has_bias) {
@@ -490,6 +494,21 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
               const float a = sid < g.pairs ? act_fn(g.act_kind, hg, hu, g.alpha, g.limit) : 0.0f;
               g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
             }
+        } else if (kG1) {  // non-gated: relu(h)^2 of each row, fp16 rows by sorted position
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int f = tile * 256 + rows[i][h];
+            const float bf = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * Npad + f]) : 0.f;
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int pos = b * g.block_m + n * 8 + 2 * tq + c;
+                const int sid = g.sorted_ids[pos];
+                const float a = sid < g.pairs ? relu2(acc[i][n][2 * h + c] * gsc + bf) : 0.0f;
+                g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
+              }
+          }
         } else {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {

@@ -27,10 +27,15 @@ struct RepackArgs {
 };
 
 // Source row of tile row r for matrix `which` (0 = w13, 1 = w2), or -1 for a
-// padding row.  w13: half 0 = gate, half 1 = up; interleaved storage keeps gate
-// i in row 2i and up i in row 2i+1.
+// padding row.  Gated w13: half 0 = gate, half 1 = up; interleaved storage keeps
+// gate i in row 2i and up i in row 2i+1.  Non-gated w13 tiles are 256
+// consecutive rows, like w2's.
 __device__ __forceinline__ int source_row(const RepackArgs& a, int which, int tile, int r) {
   const Layout& L = a.L;
+  if (which == 0 && !L.gated) {
+    const int f = tile * kTileRows + r;
+    return f < L.N ? f : -1;
+  }
   if (which == 0) {
     const int f = tile * 128 + (r & 127), half = r >> 7;
     if (f >= L.N) return -1;
@@ -51,7 +56,7 @@ __global__ void repack_codes_kernel(RepackArgs a, int which) {
   const int64_t tile_bytes = which ? L.tile2_bytes : L.tile1_bytes;
   const uint8_t* src = which ? a.w2 : a.w13;
   const int64_t src_row_bytes = red / 2;
-  const int64_t src_rows = which ? L.K : 2 * L.N;
+  const int64_t src_rows = which ? L.K : (L.gated ? 2 : 1) * (int64_t)L.N;
   for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(u % 256);
     const int j = (int)((u / 256) % 2);
@@ -100,7 +105,7 @@ __global__ void repack_scales_kernel(RepackArgs a, int which) {
   const int64_t total = (int64_t)L.E * T * chunks * 256;
   const int64_t tile_bytes = which ? L.tile2_bytes : L.tile1_bytes;
   const uint8_t* src = which ? a.w2_s : a.w13_s;
-  const int64_t src_rows = which ? L.K : 2 * L.N;
+  const int64_t src_rows = which ? L.K : (L.gated ? 2 : 1) * (int64_t)L.N;
   const int sb = L.fmt == MOE_W_INT4_U4B8 ? 2 : 1;  // source bytes per scale
   for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(u % 256);
@@ -140,17 +145,19 @@ __global__ void repack_scales_kernel(RepackArgs a, int which) {
 // Bias rows (deinterleaved, zero padded) and global scales.
 __global__ void repack_misc_kernel(RepackArgs a) {
   const Layout& L = a.L;
-  const int64_t n13 = a.has_b13 ? (int64_t)L.E * 2 * L.Npad : 0;
+  const int halves = L.gated ? 2 : 1;  // gate and up rows, or h rows only
+  const int64_t n13 = a.has_b13 ? (int64_t)L.E * halves * L.Npad : 0;
   const int64_t n2 = a.has_b2 ? (int64_t)L.E * L.Kpad2 : 0;
   const int64_t ngs = L.E;
   for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < n13 + n2 + ngs;
        u += (int64_t)gridDim.x * blockDim.x) {
     if (u < n13) {
-      const int f = (int)(u % L.Npad), half = (int)((u / L.Npad) % 2), e = (int)(u / (2LL * L.Npad));
+      const int f = (int)(u % L.Npad), half = (int)((u / L.Npad) % halves);
+      const int e = (int)(u / ((int64_t)halves * L.Npad));
       uint16_t v = 0;
       if (f < L.N) {
         const int row = a.interleaved ? 2 * f + half : half * L.N + f;
-        v = a.b13[(int64_t)e * 2 * L.N + row];
+        v = a.b13[(int64_t)e * halves * L.N + row];
       }
       reinterpret_cast<uint16_t*>(a.out + L.b13_off)[u] = v;
     } else if (u < n13 + n2) {
@@ -194,6 +201,7 @@ extern "C" int moe_repack_weights(const moe_layer_desc* desc, const void* w13, c
   if (desc->fmt == MOE_W_NVFP4 && (!w13_gs || !w2_gs)) return MOE_ERR_INVALID;
   if ((desc->has_bias13 && !b13) || (desc->has_bias2 && !b2)) return MOE_ERR_INVALID;
   if (desc->w13_interleaved && (2 * desc->inter) % 2 != 0) return MOE_ERR_INVALID;
+  if (desc->w13_interleaved && desc->non_gated) return MOE_ERR_INVALID;
   RepackArgs a;
   a.L = L;
   a.interleaved = desc->w13_interleaved != 0;

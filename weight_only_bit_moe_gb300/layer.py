@@ -19,7 +19,7 @@ import torch
 from . import binding as B
 
 FMT = {"int4": B.MOE_W_INT4_U4B8, "mxfp4": B.MOE_W_MXFP4, "nvfp4": B.MOE_W_NVFP4}
-ACT = {"silu_mul": B.MOE_ACT_SILU_MUL, "sigmoid_alpha": B.MOE_ACT_SIGMOID_ALPHA}
+ACT = {"silu_mul": B.MOE_ACT_SILU_MUL, "sigmoid_alpha": B.MOE_ACT_SIGMOID_ALPHA, "relu2": B.MOE_ACT_RELU2}
 GROUP = {"int4": 128, "mxfp4": 32, "nvfp4": 16}
 
 
@@ -48,11 +48,12 @@ class MoELayer:
     """One layer's expert bank on one GPU, repacked for the kernels."""
 
     def __init__(self, fmt: str, num_experts: int, hidden: int, inter: int, w13, w13_s, w13_gs, b13, w2, w2_s,
-                 w2_gs, b2, interleaved: bool = False, stream=None):
+                 w2_gs, b2, interleaved: bool = False, gated: bool = True, stream=None):
         self.fmt = fmt
         self.E, self.K, self.N = num_experts, hidden, inter
+        self.gated = gated  # False: w13 holds N rows and the activation is relu2
         self.desc = B.moe_layer_desc(FMT[fmt], num_experts, hidden, inter, GROUP[fmt], int(interleaved),
-                                     int(b13 is not None), int(b2 is not None))
+                                     int(b13 is not None), int(b2 is not None), int(not gated))
         dev = w13.device
         self.device = dev
         self.packed = torch.empty(B.moe_repack_size(self.desc), dtype=torch.uint8, device=dev)
@@ -65,7 +66,7 @@ class MoELayer:
         t = dict(w13=_dev(W.w13, device), w13_s=_dev(W.w13_s, device), w13_gs=_dev(W.w13_gs, device),
                  b13=_dev(W.b13, device), w2=_dev(W.w2, device), w2_s=_dev(W.w2_s, device),
                  w2_gs=_dev(W.w2_gs, device), b2=_dev(W.b2, device))
-        layer = cls(W.fmt, W.E, W.K, W.N, interleaved=W.interleaved, stream=stream, **t)
+        layer = cls(W.fmt, W.E, W.K, W.N, interleaved=W.interleaved, gated=W.gated, stream=stream, **t)
         torch.cuda.current_stream(device).synchronize()  # source tensors may be freed after this
         return layer
 
@@ -100,11 +101,13 @@ class MoELayer:
         return ws
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, a: AlignOut,
-                expert_base: int = 0, act: str = "silu_mul", alpha: float = 1.702, limit: float = math.inf,
+                expert_base: int = 0, act: Optional[str] = None, alpha: float = 1.702, limit: float = math.inf,
                 routed_scaling_factor: float = 1.0, post_norm_w: Optional[torch.Tensor] = None,
                 norm_eps: float = 1e-8, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                 stream=None) -> torch.Tensor:
         M, k = topk_ids.shape
+        if act is None:  # the layer's own kind: silu_and_mul when gated, relu2 otherwise
+            act = "silu_mul" if self.gated else "relu2"
         if out is None:
             out = torch.empty((M, self.K), dtype=torch.bfloat16, device=self.device)
         ws = workspace if workspace is not None else self.workspace(M, k, a.block_m)
