@@ -154,8 +154,9 @@ int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int blo
  *            (_expert_norm_factors / _expert_norm_sum, weight_first)
  * Non-local pairs contribute nothing.  Arithmetic: fp32 accumulation, scales,
  * bias, activation and combine; the tensor-core operands are fp16 (weights
- * dequantised exactly, x and a rounded to fp16); a is kept as fp16 and y as
- * fp32 between the kernels; only out is bf16.
+ * dequantised exactly, x and a rounded to fp16); a and y are kept as fp16
+ * between the kernels (16-bit, as the Marlin path keeps its GEMM2 output); the
+ * combine sums in fp32 and writes out as bf16.
  * Arguments (device unless said): packed from moe_repack_weights for `desc`;
  * x bf16 [M, K]; topk_ids int32 [M, top_k]; topk_weights fp32 [M, top_k];
  * sorted_ids / expert_ids / n_padded from moe_align with the same M, top_k,
@@ -165,8 +166,8 @@ int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int blo
  * out bf16 [M, K]; workspace of at least moe_workspace_size() bytes.  packed and
  * workspace must be 256-byte aligned; x, out and post_norm_w 16-byte aligned.
  * Operand range: the tensor-core operands are 16-bit (fp16 for GEMM2 and for
- * INT4's GEMM1), so inputs and activations must stay inside the fp16 range
- * (|v| < 65504); MXFP4 scales must lie in [2^-20, 2^9] (E8M0 bytes 107..136).
+ * INT4's GEMM1) and y is fp16, so inputs, activations and expert outputs must
+ * stay inside the fp16 range (|v| < 65504); MXFP4 scales must lie in [2^-20, 2^9] (E8M0 bytes 107..136).
  * M == 0 is a no-op. */
 int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void* x, int M,
                       int top_k, const int32_t* topk_ids, const float* topk_weights,

@@ -70,7 +70,7 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   w->a_off = off;
   off = round_up64(off + cap * L.Npad * 2, 256);
   w->y_off = off;
-  off = round_up64(off + pairs * L.K * 4, 256);
+  off = round_up64(off + pairs * L.K * 2, 256);  // y, bf16
   w->part1_off = off;
   off = round_up64(off + (int64_t)w->max_split1 * per1, 256);
   w->part2_off = off;
@@ -224,7 +224,7 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.alpha = alpha;
   g.limit = limit;
   g.a_out = reinterpret_cast<uint16_t*>(ws + w.a_off);
-  g.y_out = reinterpret_cast<float*>(ws + w.y_off);
+  g.y_out = reinterpret_cast<uint16_t*>(ws + w.y_off);
   g.status = reinterpret_cast<unsigned*>(ws + w.status_off);
 
   // GEMM1 + activation
@@ -256,7 +256,7 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   c.E = L.E;
   c.topk_ids = topk_ids;
   c.topk_weights = topk_weights;
-  c.y = reinterpret_cast<const float*>(ws + w.y_off);
+  c.y = reinterpret_cast<const uint16_t*>(ws + w.y_off);
   c.post_norm_w = static_cast<const uint16_t*>(post_norm_w);
   c.norm_eps = norm_eps;
   c.rsf = routed_scaling_factor;

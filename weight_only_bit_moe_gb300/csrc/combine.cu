@@ -10,9 +10,10 @@
 //              _expert_norm_sum, weight_first, eps 1e-8; non-local slots get
 //              factor 0).
 //
-// y is fp32.  Each thread owns 8 consecutive columns (two 16-byte loads per
-// slot, one 16-byte bf16 store) and issues every slot's loads before it sums,
-// in slot order.  Plain rows spread a token over a 2-D grid of 128-thread
+// y is fp16 (a 16-bit GEMM2 output, as the pages' Marlin path keeps it, with
+// fp16's 11 significant bits), summed in fp32.  Each thread owns 8 consecutive columns (one
+// 16-byte load per slot, one 16-byte bf16 store) and issues every slot's loads
+// before it sums, in slot order.  Plain rows spread a token over a 2-D grid of 128-thread
 // column blocks; post-norm rows take one CTA per token, wide enough to cover
 // the row in one pass (up to 1024 threads), so the row reduction stays in it.
 #include <cuda_runtime.h>
@@ -24,12 +25,6 @@ namespace moe {
 
 constexpr int kCols = 8;  // columns per thread
 constexpr int kMaxTopK = 16;
-
-__device__ __forceinline__ void ld8(const float* p, float (&v)[8]) {
-  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
 
 __device__ __forceinline__ void bf16x8(const uint16_t* p, float (&v)[8]) {  // 8 bf16 -> fp32
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -43,7 +38,14 @@ __device__ __forceinline__ void bf16x8(const uint16_t* p, float (&v)[8]) {  // 8
 
 // y of one pair at columns [col, col+8).
 __device__ __forceinline__ void pair_y8(const CombineArgs& c, int pair, int col, float (&v)[8]) {
-  ld8(c.y + (int64_t)pair * c.K + col, v);
+  const uint4 u = __ldcg(reinterpret_cast<const uint4*>(c.y + (int64_t)pair * c.K + col));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
 }
 
 __device__ __forceinline__ void norm_w8(const uint16_t* w, int col, float (&v)[8]) {

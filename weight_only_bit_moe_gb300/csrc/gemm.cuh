@@ -45,7 +45,6 @@
 namespace moe {
 
 constexpr int kSup = 2;                // 64-K stages per pipeline unit (one barrier round per unit)
-constexpr int kSA = 2;                 // dequantised-A ring in TMEM, in units
 constexpr int kNumDequantWarps = 8;
 constexpr int kNumEpiWarps = 8;                             // two per TMEM lane quarter
 constexpr int kEpiThreads = kNumEpiWarps * 32;
@@ -73,7 +72,7 @@ struct GemmArgs {
   int max_split;
   int split_rows;             // rows of each split-K partial slice
   uint16_t* a_out;            // GEMM1 output, fp16 [cap, Npad]
-  float* y_out;               // GEMM2 output, fp32 [pairs, K]
+  uint16_t* y_out;            // GEMM2 output, fp16 [pairs, K]
   float* partial;             // split-K partials [max_split][split_rows][width]
   int32_t* counters;          // split-K arrival counters [T * blocks]
   unsigned* status;
@@ -81,7 +80,8 @@ struct GemmArgs {
 
 template <int BN>
 struct GemmSmem {
-  static constexpr int kNacc = BN >= 128 ? 1 : 2;                                   // TMEM accumulators
+  static constexpr int kSA = 2;                    // dequantised-A ring in TMEM, in units
+  static constexpr int kNacc = BN >= 128 ? 1 : 2;  // TMEM accumulators
   static constexpr int kBUnitBytes = kSup * BN * 128;  // activation rows of a unit, [stage][row][64]
   static constexpr int kSB = BN <= 64 ? 6 : 4;           // activation ring, in units
   static constexpr int kB = 0;
@@ -121,6 +121,38 @@ __device__ __forceinline__ float act_fn(int kind, float g, float u, float alpha,
 }
 // Activation of non-gated experts: relu(h)^2.
 __device__ __forceinline__ float relu2(float h) { return h > 0.0f ? h * h : 0.0f; }
+
+// Warp transpose of 16-bit values in groups of 8 lanes, for coalesced epilogue
+// stores.  On entry lane L holds feature L's values for tokens 0..7, packed
+// w[j] = token 2j | token 2j+1 << 16; on exit it holds features (L & ~7) + 0..7
+// of token L & 7, in feature order (one 16-byte store).  Three butterfly steps
+// (lane bit i <-> token bit i), two shuffles each.
+__device__ __forceinline__ uint4 transpose8x8_u16(const uint32_t (&w)[4], int lane) {
+  const bool b0 = lane & 1, b1 = (lane >> 1) & 1, b2 = (lane >> 2) & 1;
+  // step 1: keep the tokens whose bit 0 equals lane bit 0, trade the others
+  const uint32_t keep_sel = b0 ? 0x5410u : 0x7632u;
+  const uint32_t r0 = __shfl_xor_sync(0xffffffffu, __byte_perm(w[0], w[1], keep_sel), 1);
+  const uint32_t r1 = __shfl_xor_sync(0xffffffffu, __byte_perm(w[2], w[3], keep_sel), 1);
+  const uint32_t se = b0 ? 0x3254u : 0x5410u, so = b0 ? 0x3276u : 0x7610u;
+  const uint32_t n0 = __byte_perm(w[0], r0, se), n1 = __byte_perm(w[1], r0, so);
+  const uint32_t n2 = __byte_perm(w[2], r1, se), n3 = __byte_perm(w[3], r1, so);
+  // step 2: words are tokens (t1, t2) = (j & 1, j >> 1); trade on t1
+  const uint32_t ra = __shfl_xor_sync(0xffffffffu, b1 ? n0 : n1, 2);
+  const uint32_t rb = __shfl_xor_sync(0xffffffffu, b1 ? n2 : n3, 2);
+  const uint32_t x00 = b1 ? ra : n0, x01 = b1 ? n1 : ra, x10 = b1 ? rb : n2, x11 = b1 ? n3 : rb;
+  // step 3: trade on t2
+  const uint32_t rc = __shfl_xor_sync(0xffffffffu, b2 ? x00 : x10, 4);
+  const uint32_t rd = __shfl_xor_sync(0xffffffffu, b2 ? x01 : x11, 4);
+  return b2 ? make_uint4(rc, rd, x10, x11) : make_uint4(x00, x01, rc, rd);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+}
+
+__device__ __forceinline__ void stg128(void* p, const uint4& v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 
 struct WorkPlan {
   int nb;      // valid blocks
@@ -188,7 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   constexpr bool kGated = STAGE == kGemm1Gated;  // tile halves are gate and up rows
   using SM = GemmSmem<BN>;
   using PF = PackedFmt<FMT>;
-  constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc;
+  constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc, kSA = SM::kSA;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBar);
@@ -550,29 +582,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               for (int jj = 0; jj < 8; ++jj)
                 av[jj] = act_fn(MOE_ACT_SIGMOID_ALPHA, f0[jj] * gsc + bias0, f1[jj] * gsc + bias1, g.alpha, g.limit);
             }
+            // the warp's 32 features x 8 tokens, transposed: each lane stores 8
+            // consecutive features of one token (16 bytes)
+            uint32_t w[4];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-              if (c0 + jj < jmax)
-                g.a_out[(int64_t)(pos0 + jj) * Npad + row0] = __half_as_ushort(__float2half_rn(sid[jj] < g.pairs ? av[jj] : 0.0f));
+            for (int j = 0; j < 4; ++j)
+              w[j] = pack_f16x2(sid[2 * j] < g.pairs ? av[2 * j] : 0.0f, sid[2 * j + 1] < g.pairs ? av[2 * j + 1] : 0.0f);
+            const uint4 o = transpose8x8_u16(w, lane);
+            const int tt = lane & 7;
+            if (c0 + tt < jmax) stg128(g.a_out + (int64_t)(pos0 + tt) * Npad + (row0 - hr) + q * 32 + (lane & 24), o);
           } else if (kG1) {  // non-gated: both halves are features, a = relu(h)^2
+            uint32_t w0[4], w1[4];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-              if (c0 + jj < jmax) {
-                const bool live = sid[jj] < g.pairs;
-                const float a0 = live ? relu2(f0[jj] * gsc + bias0) : 0.0f;
-                const float a1 = live ? relu2(f1[jj] * gsc + bias1) : 0.0f;
-                uint16_t* dst = g.a_out + (int64_t)(pos0 + jj) * Npad;
-                dst[row0] = __half_as_ushort(__float2half_rn(a0));
-                dst[row1] = __half_as_ushort(__float2half_rn(a1));
-              }
+            for (int j = 0; j < 4; ++j) {
+              const bool l0 = sid[2 * j] < g.pairs, l1 = sid[2 * j + 1] < g.pairs;
+              w0[j] = pack_f16x2(l0 ? relu2(f0[2 * j] * gsc + bias0) : 0.0f, l1 ? relu2(f0[2 * j + 1] * gsc + bias0) : 0.0f);
+              w1[j] = pack_f16x2(l0 ? relu2(f1[2 * j] * gsc + bias1) : 0.0f, l1 ? relu2(f1[2 * j + 1] * gsc + bias1) : 0.0f);
+            }
+            const uint4 o0 = transpose8x8_u16(w0, lane), o1 = transpose8x8_u16(w1, lane);
+            const int tt = lane & 7;
+            if (c0 + tt < jmax) {
+              uint16_t* dst = g.a_out + (int64_t)(pos0 + tt) * Npad + (row0 - hr) + q * 32 + (lane & 24);
+              stg128(dst, o0);
+              stg128(dst + 128, o1);
+            }
           } else {
+            // fp16 rows by pair, transposed like GEMM1's: each lane stores 8
+            // consecutive outputs of one pair per half; ok0/ok1 are warp-uniform
+            // (K % 64 == 0 and a warp's 32 rows start on a multiple of 32)
+            const int tt = lane & 7;
+            const int sid_t = epi_sid[c0 + tt];
+            const bool live = c0 + tt < jmax && sid_t < g.pairs;
+            uint16_t* dst = g.y_out + (int64_t)(live ? sid_t : 0) * L.K + (row0 - hr) + q * 32 + (lane & 24);
+            uint32_t w[4];
+            if (ok0) {
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-              if (c0 + jj < jmax && sid[jj] < g.pairs) {
-                float* dst = g.y_out + (int64_t)sid[jj] * L.K;
-                if (ok0) dst[row0] = f0[jj] * gsc + bias0;
-                if (ok1) dst[row1] = f1[jj] * gsc + bias1;
-              }
+              for (int j = 0; j < 4; ++j)
+                w[j] = pack_f16x2(f0[2 * j] * gsc + bias0, f0[2 * j + 1] * gsc + bias0);
+              const uint4 o = transpose8x8_u16(w, lane);
+              if (live) stg128(dst, o);
+            }
+            if (ok1) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                w[j] = pack_f16x2(f1[2 * j] * gsc + bias1, f1[2 * j + 1] * gsc + bias1);
+              const uint4 o = transpose8x8_u16(w, lane);
+              if (live) stg128(dst + 128, o);
+            }
           }
         }
       }

@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
               for (int c = 0; c < 2; ++c) {
                 const int pos = b * g.block_m + n * 8 + 2 * tq + c;
                 const int sid = g.sorted_ids[pos];
-                if (sid < g.pairs) g.y_out[(int64_t)sid * L.K + o] = acc[i][n][2 * h + c] * gsc + bo;
+                if (sid < g.pairs) g.y_out[(int64_t)sid * L.K + o] = __half_as_ushort(__float2half_rn(acc[i][n][2 * h + c] * gsc + bo));
               }
           }
         }
