@@ -4,17 +4,22 @@
 // block of the expert-parallel filter in "Marlin MoE kernel occupancy ..."
 // (sglang PR #31552), marlin_template.h).
 //
-// One CTA of 1024 threads does the whole job, which at the layer's sizes
-// (<= 32768 pairs) costs a few microseconds.  It is a stable counting sort:
-//   1. each of the 32 warps owns a contiguous segment of pairs and counts its
-//      segment's local expert ids into its own row of a [32][E] table;
-//   2. per expert, one warp scans the 32 segment counts into the expert's total
-//      and the segments' offsets; the padded totals are scanned into run
-//      starts and n_padded; every slot is pre-filled as padding;
-//   3. the offsets become absolute and the block -> expert table is written;
-//   4. each warp walks its segment in order, 32 pairs at a time: the lanes that
-//      share an expert (found with one ballot per key bit) take consecutive slots after that
-//      expert's running offset, so equal experts keep ascending pair order.
+// A stable counting sort spread over G CTAs with no communication between
+// them.  The pairs are cut into G contiguous chunks; CTA c
+//   1. counts every local pair per expert (shared-memory atomics) -- the
+//      expert totals -- and, apart, the pairs of the chunks before its own, and
+//      counts its own chunk per warp segment into a [32][E] table;
+//   2. scans the padded totals into run starts (every CTA gets the same
+//      starts) and, per expert, the segment counts into segment offsets;
+//   3. writes the padding slots, block experts and -1 blocks of the experts
+//      and ranges it owns (round-robin over CTAs), and n_padded (CTA 0);
+//   4. scatters its chunk: each warp walks its segment 32 pairs at a time; the
+//      lanes that share an expert (one ballot per key bit) take consecutive
+//      slots after that expert's running offset, so equal experts keep
+//      ascending pair order across segments and chunks.
+// Each CTA reads all ids once (L2-resident after the first), so the cost is
+// one pass over the ids per CTA plus a chunk of ~1024 pairs: a few
+// microseconds at 32768 pairs, against one CTA's ~50 walking them all.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,7 +30,8 @@ namespace moe {
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kAlignMaxExperts = 1024;
-constexpr int kAlignBatch = 16;  // rounds of 32 ids a warp loads at once
+constexpr int kAlignChunk = 1024;   // pairs scattered per CTA (the grid covers the pairs)
+constexpr int kAlignMaxCtas = 128;  // beyond this the chunks grow instead
 
 // Lanes of the warp whose key equals this lane's: one ballot per key bit (keys
 // are local expert + 1, so non-local pairs share key 0).
@@ -40,7 +46,7 @@ __device__ __forceinline__ uint32_t peer_mask(int key, int nbits) {
 }
 
 __device__ __forceinline__ int local_expert(const int32_t* ids, int p, int base, int E) {
-  const int e = ids[p] - base;
+  const int e = __ldg(ids + p) - base;
   return (e >= 0 && e < E) ? e : -1;
 }
 
@@ -51,63 +57,55 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   extern __shared__ __align__(16) unsigned char smem[];
   const int E = num_experts;
   const int Ep = E + 1;                     // row stride: column walks hit distinct banks
-  int* tab = reinterpret_cast<int*>(smem);  // [32][Ep] segment counts, then segment offsets
-  int* count = tab + kAlignWarps * Ep;      // [E]
-  int* start = count + E;                   // [E]
+  int* tab = reinterpret_cast<int*>(smem);  // [32][Ep] segment counts, then absolute offsets
+  int* total = tab + kAlignWarps * Ep;      // [E] local pairs per expert
+  int* before = total + E;                  // [E] ... in the chunks before this CTA's
+  int* start = before + E;                  // [E] padded run start
   __shared__ int warp_sums[32];
 
   grid_dependency_wait();
   grid_dependents_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int seg = (pairs + kAlignWarps - 1) / kAlignWarps;
-  const int p0 = warp * seg, p1 = min(pairs, p0 + seg);
+  const int G = gridDim.x, c = blockIdx.x;
+  const int chunk = (pairs + G - 1) / G;
+  const int q0 = min(pairs, c * chunk), q1 = min(pairs, q0 + chunk);
+  const int seg = (q1 - q0 + kAlignWarps - 1) / kAlignWarps;
+  const int p0 = min(q1, q0 + warp * seg), p1 = min(q1, p0 + seg);
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int key_bits = 32 - __clz(E);  // keys 0..E
   int* row = tab + warp * Ep;
 
-  // 1. segment counts; a warp loads up to kAlignBatch rounds of 32 ids at once
-  //    (one round trip), then counts them.  A segment that fits one batch keeps
-  //    its ids in registers for the scatter.
-  for (int e = lane; e < E; e += 32) row[e] = 0;
-  __syncwarp();
-  const bool one_batch = p1 - p0 <= 32 * kAlignBatch;
-  int keep[kAlignBatch];
-  for (int pass = p0; pass < p1; pass += 32 * kAlignBatch) {
-    int ev[kAlignBatch];
+  for (int i = tid; i < kAlignWarps * Ep + 2 * E; i += kAlignThreads) tab[i] = 0;
+  __syncthreads();
+
+  // 1. expert totals and the counts of the earlier chunks (every id, one pass;
+  //    eight loads in flight per thread before their atomics)
+  constexpr int kBatch = 8;
+  for (int pass = 0; pass < pairs; pass += kBatch * kAlignThreads) {
+    int ev[kBatch];
 #pragma unroll
-    for (int i = 0; i < kAlignBatch; ++i) {
-      const int p = pass + 32 * i + lane;
-      ev[i] = p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1;
-      keep[i] = ev[i];
+    for (int i = 0; i < kBatch; ++i) {
+      const int p = pass + i * kAlignThreads + tid;
+      ev[i] = p < pairs ? local_expert(topk_ids, p, expert_base, E) : -1;
     }
 #pragma unroll
-    for (int i = 0; i < kAlignBatch; ++i) {
-      if (pass + 32 * i >= p1) break;
-      const uint32_t m = peer_mask(ev[i] + 1, key_bits);
-      if (ev[i] >= 0 && (m & lt_mask) == 0) row[ev[i]] += __popc(m);
-      __syncwarp();
+    for (int i = 0; i < kBatch; ++i) {
+      if (ev[i] >= 0) {
+        atomicAdd(&total[ev[i]], 1);
+        if (pass + i * kAlignThreads + tid < q0) atomicAdd(&before[ev[i]], 1);
+      }
     }
+  }
+  //    this warp's segment, per expert
+  for (int p = p0 + lane; p < p1; p += 32) {
+    const int e = local_expert(topk_ids, p, expert_base, E);
+    if (e >= 0) atomicAdd(&row[e], 1);
   }
   __syncthreads();
 
-  // 2. per expert, one warp scans the 32 segment counts (lane = segment): the
-  //    expert's total and each segment's offset inside the expert's run
-  for (int e = warp; e < E; e += kAlignWarps) {
-    const int v = tab[lane * Ep + e];
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
-    }
-    tab[lane * Ep + e] = incl - v;
-    if (lane == 31) count[e] = incl;
-  }
-  __syncthreads();
-
-  //    padded scan over experts (E <= 1024: one expert per thread)
-  const int c = tid < E ? count[tid] : 0;
-  const int padded = (c + block_m - 1) / block_m * block_m;
+  // 2. padded scan over experts (E <= 1024: one expert per thread) ...
+  const int cnt = tid < E ? total[tid] : 0;
+  const int padded = (cnt + block_m - 1) / block_m * block_m;
   int incl = padded;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -115,6 +113,17 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     if (lane >= o) incl += v;
   }
   if (lane == 31) warp_sums[warp] = incl;
+  //    ... and, per expert, one warp scans the 32 segment counts (lane = segment)
+  for (int e = warp; e < E; e += kAlignWarps) {
+    const int v = tab[lane * Ep + e];
+    int s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
+    }
+    tab[lane * Ep + e] = s - v + before[e];  // offset of the segment inside the expert's run
+  }
   __syncthreads();
   if (warp == 0) {
     int sum = warp_sums[lane];
@@ -126,46 +135,42 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     warp_sums[lane] = sum;  // inclusive over warps
   }
   __syncthreads();
-  const int total = warp_sums[31];
+  const int n_total = warp_sums[31];
   if (tid < E) start[tid] = incl - padded + (warp ? warp_sums[warp - 1] : 0);
-  if (tid == 0) *n_padded = total;
-  // every slot starts as padding and every block as -1; real entries and block
-  // experts overwrite them after the barrier
-  const int32_t sentinel = pairs;
-  for (int64_t i = tid; i < cap; i += kAlignThreads) sorted_ids[i] = sentinel;
-  for (int64_t b = tid; b < cap / block_m; b += kAlignThreads) expert_ids[b] = -1;
+  if (c == 0 && tid == 0) *n_padded = n_total;
   __syncthreads();
 
-  // 3. absolute offsets of each segment; block -> expert
+  // 3. padding slots and block experts of the experts this CTA owns; the tail
+  //    past n_padded (sentinel slots, -1 blocks) split over all CTAs
+  //    (one warp per expert: a thread's global stores issue one after another,
+  //    so the experts' stores go out from different warps side by side)
+  const int32_t sentinel = pairs;
+  for (int e = c + warp * G; e < E; e += kAlignWarps * G) {
+    const int s0 = start[e], n = total[e];
+    const int pe = (n + block_m - 1) / block_m * block_m;
+    for (int i = s0 + n + lane; i < s0 + pe; i += 32) sorted_ids[i] = sentinel;
+    for (int b = s0 / block_m + lane; b < (s0 + pe) / block_m; b += 32) expert_ids[b] = e;
+  }
+  for (int64_t i = n_total + (int64_t)c * kAlignThreads + tid; i < cap; i += (int64_t)G * kAlignThreads)
+    sorted_ids[i] = sentinel;
+  for (int64_t b = n_total / block_m + (int64_t)c * kAlignThreads + tid; b < cap / block_m;
+       b += (int64_t)G * kAlignThreads)
+    expert_ids[b] = -1;
   for (int idx = tid; idx < kAlignWarps * E; idx += kAlignThreads) {
     const int w = idx / E, e = idx - w * E;
     tab[w * Ep + e] += start[e];
   }
-  for (int e = tid; e < E; e += kAlignThreads) {
-    const int s0 = start[e];
-    const int pe = (count[e] + block_m - 1) / block_m * block_m;
-    for (int b = s0 / block_m; b < (s0 + pe) / block_m; ++b) expert_ids[b] = e;
-  }
   __syncthreads();
 
-  // 4. stable scatter of each segment, rounds in pair order
-  for (int pass = p0; pass < p1; pass += 32 * kAlignBatch) {
-    int ev[kAlignBatch];
-#pragma unroll
-    for (int i = 0; i < kAlignBatch; ++i) {
-      const int p = pass + 32 * i + lane;
-      ev[i] = one_batch ? keep[i] : (p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1);
-    }
-#pragma unroll
-    for (int i = 0; i < kAlignBatch; ++i) {
-      if (pass + 32 * i >= p1) break;
-      const int e = ev[i];
-      const uint32_t m = peer_mask(e + 1, key_bits);
-      if (e >= 0) sorted_ids[row[e] + __popc(m & lt_mask)] = pass + 32 * i + lane;
-      __syncwarp();
-      if (e >= 0 && (m & lt_mask) == 0) row[e] += __popc(m);
-      __syncwarp();
-    }
+  // 4. stable scatter of this warp's segment, rounds in pair order
+  for (int pass = p0; pass < p1; pass += 32) {
+    const int p = pass + lane;
+    const int e = p < p1 ? local_expert(topk_ids, p, expert_base, E) : -1;
+    const uint32_t m = peer_mask(e + 1, key_bits);
+    if (e >= 0) sorted_ids[row[e] + __popc(m & lt_mask)] = p;
+    __syncwarp();
+    if (e >= 0 && (m & lt_mask) == 0) row[e] += __popc(m);
+    __syncwarp();
   }
 }
 
@@ -189,19 +194,22 @@ extern "C" int moe_align(const int32_t* topk_ids, int M, int top_k, int expert_b
   if ((int64_t)M * top_k >= (int64_t)1 << 31) return MOE_ERR_INVALID;
   if (!sorted_ids || !expert_ids || !n_padded || (M > 0 && !topk_ids)) return MOE_ERR_INVALID;
   const int64_t cap = moe_align_capacity(M, top_k, num_experts, block_m);
-  const size_t smem = ((size_t)kAlignWarps * (num_experts + 1) + 2 * (size_t)num_experts) * 4;
+  const int pairs = M * top_k;
+  const size_t smem = ((size_t)kAlignWarps * (num_experts + 1) + 3 * (size_t)num_experts) * 4;
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   if (!configured[dev]) {
     if (cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(((size_t)kAlignWarps * (kAlignMaxExperts + 1) + 2 * (size_t)kAlignMaxExperts) * 4)) !=
+                             (int)(((size_t)kAlignWarps * (kAlignMaxExperts + 1) + 3 * (size_t)kAlignMaxExperts) * 4)) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     configured[dev] = true;
   }
-  const cudaError_t err = launch_dependent(align_kernel, dim3(1), dim3(kAlignThreads), smem, (cudaStream_t)stream,
-                                           topk_ids, M * top_k, expert_base, num_experts, block_m, cap, sorted_ids,
+  int ctas = (pairs + kAlignChunk - 1) / kAlignChunk;
+  ctas = ctas < 1 ? 1 : (ctas > kAlignMaxCtas ? kAlignMaxCtas : ctas);
+  const cudaError_t err = launch_dependent(align_kernel, dim3(ctas), dim3(kAlignThreads), smem, (cudaStream_t)stream,
+                                           topk_ids, pairs, expert_base, num_experts, block_m, cap, sorted_ids,
                                            expert_ids, n_padded);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
