@@ -218,3 +218,14 @@ def test_forward_smallest_shapes(fmt, K, N):
     for B in (8, 64):
         out = run_layer(_layer(W), wl, X, block_m=B)
         check_close(out.float().cpu().numpy(), bf16_to_f32(oracle.forward_workload(wl, W, X)), f"{fmt} K={K} N={N} B={B}")
+
+
+def test_non_gated_workspace_is_smaller():
+    # relu2 banks keep N partial columns for GEMM1's split-K instead of 2N (the
+    # workspace plan reads the device's SM count, hence a GPU test)
+    from weight_only_bit_moe_gb300 import binding as B
+    D = B.moe_layer_desc
+    for M in (1, 123, 2304):
+        g = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 0), M, 2, 16)
+        ng = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 1), M, 2, 16)
+        assert 0 < ng < g, (M, g, ng)

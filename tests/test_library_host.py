@@ -68,6 +68,17 @@ def test_non_gated_layout_rules(lib):
             lib.moe_repack_size(bad)
 
 
+def test_binding_struct_matches_header(lib):
+    """The ctypes moe_layer_desc has the header struct's fields, in order, all int32."""
+    text = open(os.path.join(ROOT, "include", "moe_w4a16.h")).read()
+    body = re.search(r"typedef struct moe_layer_desc \{(.*?)\} moe_layer_desc;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"int32_t\s+(\w+)\s*;", body)
+    assert fields == [f for f, _ in lib.moe_layer_desc._fields_]
+    assert all(t is ctypes.c_int32 for _, t in lib.moe_layer_desc._fields_)
+    assert ctypes.sizeof(lib.moe_layer_desc) == 4 * len(fields)
+
+
 def test_rejects_bad_arguments_without_device(lib):
     L = lib.load()
     # align: bad block_m, too many experts, null outputs -> MOE_ERR_INVALID before any CUDA call

@@ -163,8 +163,10 @@ cudaError_t launch_combine(const CombineArgs& c, cudaStream_t st) {
   if (c.M == 0) return cudaSuccess;
   if (c.top_k > kMaxTopK || c.K % kCols) return cudaErrorInvalidValue;
   const int chunks = c.K / kCols;
-  if (!c.post_norm_w)  // plain rows: a 2-D grid of 128-thread column blocks
-    return launch_dependent(combine_kernel, dim3(c.M, (chunks + 127) / 128), dim3(128), 0, st, c);
+  if (!c.post_norm_w) {  // plain rows: a 2-D grid of column blocks of up to 128 threads, none idle at small K
+    const int threads = chunks < 128 ? (chunks + 31) / 32 * 32 : 128;
+    return launch_dependent(combine_kernel, dim3(c.M, (chunks + threads - 1) / threads), dim3(threads), 0, st, c);
+  }
   int threads = (chunks + 31) / 32 * 32;
   if (threads > 1024) threads = 1024;
   return launch_dependent(combine_kernel, dim3(c.M), dim3(threads), 0, st, c);

@@ -162,11 +162,11 @@ struct WorkPlan {
   int items;
 };
 
-__device__ __forceinline__ WorkPlan make_plan(const GemmArgs& g, bool gated) {
+__device__ __forceinline__ WorkPlan make_plan(const GemmArgs& g, bool gemm1) {
   WorkPlan p;
   p.nb = *g.n_padded / g.block_m;
-  p.T = gated ? g.L.T1 : g.L.T2;
-  const int stages = gated ? g.L.S1 : g.L.S2;
+  p.T = gemm1 ? g.L.T1 : g.L.T2;
+  const int stages = gemm1 ? g.L.S1 : g.L.S2;
   p.units = stages / g.L.period;
   const int base = p.T * p.nb;
   const int grid = (int)gridDim.x;

@@ -58,11 +58,11 @@ struct SmallSmem {
 // Split-K choice in units of 1/8 stage: each wave streams ceil(units/S)
 // scale periods; a split item also writes its fp32 partial (256 rows x BN x 4 B
 // = BN/8 stages) and the last CTA of each item reads S of them back.
-__device__ __forceinline__ WorkPlan make_plan_small(const GemmArgs& g, bool gated, int bn) {
+__device__ __forceinline__ WorkPlan make_plan_small(const GemmArgs& g, bool gemm1, int bn) {
   WorkPlan p;
   p.nb = *g.n_padded / g.block_m;
-  p.T = gated ? g.L.T1 : g.L.T2;
-  const int stages = gated ? g.L.S1 : g.L.S2;
+  p.T = gemm1 ? g.L.T1 : g.L.T2;
+  const int stages = gemm1 ? g.L.S1 : g.L.S2;
   p.units = stages / g.L.period;
   const int base = p.T * p.nb;
   const int grid = (int)gridDim.x;
