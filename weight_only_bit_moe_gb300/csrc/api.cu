@@ -70,7 +70,7 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   w->a_off = off;
   off = round_up64(off + cap * L.Npad * 2, 256);
   w->y_off = off;
-  off = round_up64(off + pairs * L.K * 2, 256);  // y, bf16
+  off = round_up64(off + pairs * L.K * 2, 256);  // y, fp16
   w->part1_off = off;
   off = round_up64(off + (int64_t)w->max_split1 * per1, 256);
   w->part2_off = off;
