@@ -2,6 +2,7 @@
 // the workspace plan and the forward's launch sequence (GEMM1 + activation ->
 // GEMM2 -> combine), all enqueued on the caller's stream without host syncs.
 #include <cuda.h>
+#include <cmath>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -133,13 +134,37 @@ inline cudaError_t trace(int i, cudaStream_t st) {
 
 using namespace moe;
 
+namespace moe {
+
+// Expected token blocks of size B one expert occupies when its row count is
+// Poisson(lambda): the sum over n >= 1 of P(n) * ceil(n / B).
+static double expected_blocks(double lambda, int B) {
+  double p = std::exp(-lambda), e = 0.0;  // p = P(n), from P(0)
+  const int nmax = (int)(lambda + 12.0 * std::sqrt(lambda + 1.0)) + 16;
+  for (int n = 1; n <= nmax; ++n) {
+    p *= lambda / n;
+    e += p * ((n + B - 1) / B);
+  }
+  return e;
+}
+
+}  // namespace moe
+
 extern "C" int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, int num_routed_ids) {
   if (!desc || M < 0 || top_k <= 0 || num_routed_ids <= 0) return MOE_ERR_INVALID;
   // expected rows per local expert: routed pairs spread over the routed id range
   const double rows = (double)M * top_k / (double)num_routed_ids;
-  if (rows <= 8.0) return 8;
-  if (rows <= 16.0) return 16;
-  if (rows <= 32.0) return 32;
+  if (rows <= 32.0) {
+    // register-fed decode kernel: every token block streams (and dequantises)
+    // its expert's weights once, so the cost is the expected number of blocks
+    // times a block's cost relative to a 16-token block, measured on GB300:
+    // 0.86 at 8 tokens, 1.34 (FP4) or 1.56 (INT4, heavier dequantisation) at 32
+    const double cost32 = desc->fmt == MOE_W_INT4_U4B8 ? 1.56 : 1.34;
+    const double c8 = 0.86 * expected_blocks(rows, 8), c16 = expected_blocks(rows, 16),
+                 c32 = cost32 * expected_blocks(rows, 32);
+    if (c8 <= c16 && c8 <= c32) return 8;
+    return c16 <= c32 ? 16 : 32;
+  }
   // 128-token tiles keep one accumulator in tensor memory, so the epilogue does
   // not overlap the next tile's MMAs; below 1024 (16 K-stages per tile) that
   // epilogue costs more than the 64-token tiles' lower MMA rate
