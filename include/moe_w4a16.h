@@ -226,6 +226,15 @@ int moe_get_status(void* workspace, void* stream);
  * Returns MOE_ERR_INVALID for any other n. */
 int moe_set_trace_events(void* const* events, int n);
 
+/* Test hook of the device failure path.  With on != 0, every later forward
+ * whose GEMMs run the register-fed kernel (block_m 8, 16 or 32) makes CTA 0 of
+ * each GEMM end with a bounded wait on a barrier nothing arrives on: the wait
+ * gives up after its limit (2 s), records MOE_ERR_TIMEOUT in the workspace
+ * status word and the kernel ends normally, so moe_get_status reports the
+ * timeout and the context stays usable.  Outputs are computed as usual.  0
+ * turns it off.  Process-wide, not thread-safe; returns MOE_OK. */
+int moe_set_test_starve_wait(int on);
+
 /* Short English name of a status code (static storage). */
 const char* moe_status_string(int status);
 

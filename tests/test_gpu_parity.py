@@ -229,3 +229,26 @@ def test_non_gated_workspace_is_smaller():
         g = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 0), M, 2, 16)
         ng = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 1), M, 2, 16)
         assert 0 < ng < g, (M, g, ng)
+
+
+def test_device_wait_timeout_is_reported():
+    # The failure path without a fault: with the test hook on, CTA 0 of each
+    # register-fed GEMM ends with a bounded wait that nothing completes.  The
+    # wait runs out (2 s), the status word reports MOE_ERR_TIMEOUT, the outputs
+    # are still right, and the next forward runs clean on the same context.
+    from weight_only_bit_moe_gb300 import binding as B
+    wl = GPU_SMALL["int4-zipf-small"]
+    W = wk.make_weights(wl, 131)
+    X = wk.make_batch(wl, 20, 132)
+    layer = _layer(W)
+    ref = bf16_to_f32(oracle.forward_workload(wl, W, X))
+    B.moe_set_test_starve_wait(True)
+    try:
+        out = run_layer(layer, wl, X, block_m=8)
+    finally:
+        B.moe_set_test_starve_wait(False)
+    assert layer.status() == B.MOE_ERR_TIMEOUT
+    check_close(out.float().cpu().numpy(), ref, "starved run")
+    out = run_layer(layer, wl, X, block_m=8)
+    assert layer.status() == B.MOE_OK
+    check_close(out.float().cpu().numpy(), ref, "clean run after the timeout")

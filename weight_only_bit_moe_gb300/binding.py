@@ -21,7 +21,7 @@ MOE_ACT_SILU_MUL, MOE_ACT_SIGMOID_ALPHA, MOE_ACT_RELU2 = 0, 1, 2
 
 EXPORTED = ("moe_repack_size", "moe_repack_weights", "moe_align_capacity", "moe_align", "moe_choose_block_m",
             "moe_workspace_size", "moe_w4a16_forward", "moe_w4a16_forward_noalloc", "moe_get_status",
-            "moe_set_trace_events", "moe_status_string")
+            "moe_set_trace_events", "moe_set_test_starve_wait", "moe_status_string")
 MOE_NOALLOC_SCRATCH_BYTES = 64 << 20  # fixed workspace of moe_w4a16_forward_noalloc
 
 
@@ -67,6 +67,7 @@ def load(path: str = ""):
                                                     p, f32, p, p]),
                 "moe_get_status": (i32, [p, p]),
                 "moe_set_trace_events": (i32, [ctypes.POINTER(ctypes.c_void_p), i32]),
+                "moe_set_test_starve_wait": (i32, [i32]),
                 "moe_status_string": (ctypes.c_char_p, [i32]),
             }
             for name, (res, args) in sig.items():
@@ -184,3 +185,8 @@ def moe_set_trace_events(events) -> None:
         handles.append(ev.cuda_event)
     arr = (ctypes.c_void_p * len(handles))(*handles)
     _check("moe_set_trace_events", load().moe_set_trace_events(arr, len(handles)))
+
+
+def moe_set_test_starve_wait(on: bool) -> None:
+    """Test hook of the device failure path (see include/moe_w4a16.h)."""
+    _check("moe_set_test_starve_wait", load().moe_set_test_starve_wait(1 if on else 0))

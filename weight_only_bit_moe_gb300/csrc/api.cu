@@ -19,6 +19,8 @@ namespace moe {
 constexpr int64_t kSplitBudgetBytes = 64ll << 20;  // cap on each split-K partial area
 constexpr int kMaxSplit = 16;
 
+std::atomic<int> g_test_starve_wait{0};  // moe_set_test_starve_wait
+
 int device_sm_count() {
   static int cache[64] = {};
   int dev = 0;
@@ -251,6 +253,7 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.a_out = reinterpret_cast<uint16_t*>(ws + w.a_off);
   g.y_out = reinterpret_cast<uint16_t*>(ws + w.y_off);
   g.status = reinterpret_cast<unsigned*>(ws + w.status_off);
+  g.test_starve_wait = g_test_starve_wait.load(std::memory_order_relaxed);
 
   // GEMM1 + activation
   g.has_bias = desc->has_bias13 != 0;
@@ -387,6 +390,11 @@ extern "C" int moe_get_status(void* workspace, void* stream) {
   if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
   if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+extern "C" int moe_set_test_starve_wait(int on) {
+  g_test_starve_wait.store(on ? 1 : 0, std::memory_order_relaxed);
   return MOE_OK;
 }
 

@@ -76,6 +76,7 @@ struct GemmArgs {
   float* partial;             // split-K partials [max_split][split_rows][width]
   int32_t* counters;          // split-K arrival counters [T * blocks]
   unsigned* status;
+  int test_starve_wait;       // test hook (register-fed kernel): CTA 0 ends with a wait nothing completes
 };
 
 template <int BN>

@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
   uint64_t* empty = full + kSlots;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + SM::kMisc);  // [1] abort, [2] last-arrival flag
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[1]);
+  uint64_t* starve = reinterpret_cast<uint64_t*>(&misc[4]);  // test hook's barrier (never arrived on)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Layout& L = g.L;
@@ -258,6 +259,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       mbar_init(&empty[i], kSmallConsumerWarps);
     }
     misc[1] = 0;
+    mbar_init(starve, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0)
@@ -527,6 +529,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         }
       }
     }
+    // Test hook of the failure path: after all its work, CTA 0's consumers wait
+    // on a barrier nothing arrives on.  The bounded wait gives up after the wait
+    // limit, records the timeout in the status word and the kernel ends
+    // normally, so the host reads MOE_ERR_TIMEOUT and the context stays usable.
+    if (g.test_starve_wait && blockIdx.x == 0) mbar_wait(starve, 0, abort_flag, g.status);
   }
   __syncthreads();
 }
