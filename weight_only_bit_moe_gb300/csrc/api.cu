@@ -141,6 +141,7 @@ namespace moe {
 // Expected token blocks of size B one expert occupies when its row count is
 // Poisson(lambda): the sum over n >= 1 of P(n) * ceil(n / B).
 static double expected_blocks(double lambda, int B) {
+  if (lambda > 200.0) return lambda / B + 0.5;  // the rounding up adds half a block on average
   double p = std::exp(-lambda), e = 0.0;  // p = P(n), from P(0)
   const int nmax = (int)(lambda + 12.0 * std::sqrt(lambda + 1.0)) + 16;
   for (int n = 1; n <= nmax; ++n) {
@@ -156,22 +157,34 @@ extern "C" int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, 
   if (!desc || M < 0 || top_k <= 0 || num_routed_ids <= 0) return MOE_ERR_INVALID;
   // expected rows per local expert: routed pairs spread over the routed id range
   const double rows = (double)M * top_k / (double)num_routed_ids;
-  if (rows <= 32.0) {
-    // register-fed decode kernel: every token block streams (and dequantises)
-    // its expert's weights once, so the cost is the expected number of blocks
-    // times a block's cost relative to a 16-token block, measured on GB300:
-    // 0.86 at 8 tokens, 1.34 (FP4) or 1.56 (INT4, heavier dequantisation) at 32
-    const double cost32 = desc->fmt == MOE_W_INT4_U4B8 ? 1.56 : 1.34;
-    const double c8 = 0.86 * expected_blocks(rows, 8), c16 = expected_blocks(rows, 16),
-                 c32 = cost32 * expected_blocks(rows, 32);
-    if (c8 <= c16 && c8 <= c32) return 8;
-    return c16 <= c32 ? 16 : 32;
+  // Every token block streams (and dequantises) its expert's weights once, so a
+  // block size costs the expected number of blocks (Poisson rows per expert)
+  // times one block's cost.  Block costs relative to a 16-token block of the
+  // register-fed kernel, measured on GB300 at K = 2880..4096:
+  //                      8     16    32 (register-fed)   64    128 (tcgen05)
+  //   INT4              0.86  1     1.56                1.32  1.68
+  //   MXFP4             0.86  1     1.34                0.93  1.09
+  //   NVFP4             0.86  1     1.34                1.08  1.26
+  // Below K = 1024 the tcgen05 tiles are too short for those costs: the
+  // register-fed sizes serve up to 32 rows and 64-token tiles the rest (with
+  // 128-token tiles the epilogue, which does not overlap the next tile's MMAs
+  // there, outweighs the better MMA rate).
+  const bool int4 = desc->fmt == MOE_W_INT4_U4B8, mx = desc->fmt == MOE_W_MXFP4;
+  const int sizes[5] = {8, 16, 32, 64, 128};
+  const double cost[5] = {0.86, 1.0, int4 ? 1.56 : 1.34, int4 ? 1.32 : (mx ? 0.93 : 1.08),
+                          int4 ? 1.68 : (mx ? 1.09 : 1.26)};
+  const bool short_k = desc->hidden < 1024;
+  if (short_k && rows > 32.0) return 64;
+  int best = 8;
+  double best_cost = 0.0;
+  for (int i = 0; i < (short_k ? 3 : 5); ++i) {
+    const double c = cost[i] * expected_blocks(rows, sizes[i]);
+    if (i == 0 || c < best_cost) {
+      best = sizes[i];
+      best_cost = c;
+    }
   }
-  // 128-token tiles keep one accumulator in tensor memory, so the epilogue does
-  // not overlap the next tile's MMAs; below 1024 (16 K-stages per tile) that
-  // epilogue costs more than the 64-token tiles' lower MMA rate
-  if (rows <= 96.0 || desc->hidden < 1024) return 64;
-  return 128;
+  return best;
 }
 
 extern "C" int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int block_m) {
