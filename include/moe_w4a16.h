@@ -12,7 +12,8 @@
  *     fused_marlin_moe(...) with per-expert bias (kHasBias) and the
  *     expert-parallel block filter (kIsEP), and the per-expert reference loop of
  *     test_fused_marlin_moe_large_non_ep_schedule (top-k weights applied in the
- *     combine, tolerance |out - ref| <= 0.06 + 0.04 |ref|);
+ *     combine, tolerance |out - ref| <= 0.06 + 0.04 |ref|), including its
+ *     non-gated experts (is_gated=False, activation "relu2");
  *   - "SM120 MXFP4 MoE ... Marlin" (sglang PR #28231): MXFP4 weights with GPT-OSS
  *     interleaved gate/up rows (deinterleave_moe_mxfp4_w13_for_marlin), zero
  *     padding of the intermediate dimension (_pad_w13/_pad_w2), the sigmoid-alpha
@@ -27,7 +28,8 @@
  *     entry point says so.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     All device work is enqueued on it, in order.
- *   - Every entry point returns a moe_status.  Argument errors that the host can
+ *   - Every entry point returns a moe_status (size queries return -1 for
+ *     invalid arguments, the status-name lookup a string).  Argument errors that the host can
  *     see are returned synchronously and nothing is enqueued.  Errors found on the
  *     device (a bounded wait that ran out) are recorded in the workspace status
  *     word and reported by moe_get_status().
