@@ -124,6 +124,8 @@ SMALL = {
     "int4-relu2-small": dataclasses.replace(wk.WORKLOADS["int4-relu2"], K=256, N=256, E=4, Ms=(11,)),
     "nvfp4-relu2-small": dataclasses.replace(wk.WORKLOADS["int4-relu2"], fmt="nvfp4", K=64, N=48, E=4,
                                              Ms=(9,)),
+    "mxfp4-relu2-small": dataclasses.replace(wk.WORKLOADS["int4-relu2"], fmt="mxfp4", K=96, N=64, E=4,
+                                             Ms=(7,)),
 }
 
 
