@@ -6,7 +6,7 @@ none of the layer's arithmetic: no dequantisation, no GEMM, no activation, no
 routing alignment and no combine. Both the CPU oracle (through the tests and the
 benchmark) and the CUDA path are fed from the arrays returned here.
 
-The five workloads follow the problem statements on the source pages:
+The workloads follow the problem statements on the source pages:
 
 * ``tiny-int4``       the small int4 case (K=256, N=128, E=8, top_k=2).
 * ``int4-bias``       the int4 shape of the large-M schedule test in
@@ -19,13 +19,14 @@ The five workloads follow the problem statements on the source pages:
 * ``nvfp4-ep-norm``   one EP8 rank of the Muse Spark NVFP4 expert path with the
                       post-expert norm, "013-moe-middle-tiles.py" (``Weights``,
                       ``Config``, ``Inputs``).
-* ``int4-skew``       int4 K=4096, N=1536, E=128, top_k=8 with uniform or Zipf(1.2)
-                      routing.
+* ``int4-skew`` / ``int4-uniform``  int4 K=4096, N=1536, E=128, top_k=8 with
+                      Zipf(1.2) or uniform routing.
 * ``int4-relu2``      the PR #31552 test shape as that test writes it: non-gated
                       experts (w1 [E, N, K]) with relu(h)^2, x = randn/10, bias
                       = randn/100.
 
-Distributions not fixed by the pages (stated here once): x ~ N(0,1) in bf16;
+Distributions not fixed by the pages (stated here once): x ~ N(0,1) in bf16
+(times the workload's x_scale);
 routing ids distinct per token (Gumbel-top-k over the routing distribution);
 top-k weights = softmax over the k slots of N(0,1) logits, in fp32; NVFP4 global
 scales ~ U[0.008, 0.012].
