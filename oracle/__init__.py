@@ -85,6 +85,10 @@ def lib():
             L.orc_ffn_pair.argtypes = [ctypes.POINTER(_Layer), ctypes.POINTER(_Batch), i32, i32, p, p, p]
             L.orc_num_threads.restype = i32
             L.orc_num_threads.argtypes = []
+            L.orc_e4m3_encode.restype = ctypes.c_uint8
+            L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            L.orc_requant.restype = i32
+            L.orc_requant.argtypes = [p, p, i64, i64, i64, p, i32, i32, i32, i32, ctypes.c_float, p]
             _lib = L
     return _lib
 
@@ -226,3 +230,32 @@ def num_threads() -> int:
 def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:
     """uint16 bf16 bits -> float32 values (shifts into the high half)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ requant (W4AFP8 activations)
+
+def e4m3_encode(v: float) -> int:
+    """fp32 value -> E4M3 byte: nearest, ties to even, saturating at +-448."""
+    return int(lib().orc_e4m3_encode(float(v)))
+
+
+def requant(x: np.ndarray, scale: np.ndarray, masked_m: np.ndarray, tensor_scale: float, group: int = 128,
+            scale_strides: Optional[Sequence[int]] = None, out: Optional[np.ndarray] = None) -> np.ndarray:
+    """Per-token -> per-tensor FP8 requantisation (see moe_oracle.c, orc_requant).
+
+    x uint8 E4M3 [E, max_m, K]; scale: a contiguous fp32 buffer in which entry
+    (e, g, m) sits at e*se + g*sg + m*sm, (se, sg, sm) = ``scale_strides``
+    (default: [E, K/group, max_m], group-major per expert); masked_m int32 [E].
+    Rows at or past masked_m keep ``out``'s bytes (zeros when ``out`` is None)."""
+    x = np.ascontiguousarray(x, dtype=np.uint8)
+    E, max_m, K = x.shape
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    if scale_strides is None:
+        scale_strides = ((K // group) * max_m, max_m, 1)
+    se, sg, sm = (int(v) for v in scale_strides)
+    mm = np.ascontiguousarray(masked_m, dtype=np.int32)
+    res = np.zeros_like(x) if out is None else np.array(out, dtype=np.uint8, copy=True)
+    if lib().orc_requant(_ptr(x), _ptr(scale), se, sg, sm, _ptr(mm), E, max_m, K, group, float(tensor_scale),
+                         _ptr(res)) != 0:
+        raise ValueError("oracle requant rejected its arguments")
+    return res

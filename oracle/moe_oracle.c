@@ -42,6 +42,16 @@
  *                 inv = 1 / sqrt(sum_c z^2 / K + eps),
  *                 out[t] = bf16(rsf * sum_j w[t,j] * inv_j * z_j).
  *
+ *   requant     the W4AFP8 activation requantisation of "W4AFP8 requant ..." (sglang
+ *               PR #35760, _fp8_per_token_quant_to_per_tensor_quant_kernel and
+ *               _requant_row): every valid row m < masked_m[e] of each expert's FP8
+ *               payload, quantised with one fp32 scale per (row, 128-group), is
+ *               re-quantised to one per-tensor scale S:
+ *                 out = e4m3(fp32(fp32(x * s[e, g, m]) * r)),  r = fp32(1 / S),
+ *               two fp32 multiplies per element as the page states, e4m3 rounding
+ *               to nearest (ties to even) and saturating at +-448, NaN -> 0x7F;
+ *               rows at or past masked_m are left untouched.
+ *
  * h, a and y are carried exactly (fp64); the only rounding is the bf16 output.
  * The bf16 intermediates of kernel_fn (cache1 / cache2 / cache3) are that
  * implementation's storage, not part of the layer's definition, which is the
@@ -377,5 +387,55 @@ int orc_ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, double* h
                 (const uint8_t*)L->w2_s + (long)e * K * (N / L->group) * sb, K, N, L->group, NULL, W2);
     ffn_pair(L, X, e, t, W13, W2, h, a, y);
     free(W13); free(W2); free(rmap);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ requant */
+
+/* fp32 -> FP8 E4M3 (fn): the nearest of the 126 positive finite values (and 0),
+ * ties to the even code (the even mantissa), magnitudes of 448 and above
+ * saturating to 448, the sign kept (negative values that round to zero give
+ * 0x80), NaN giving 0x7F.  A brute-force search over the format's own values. */
+uint8_t orc_e4m3_encode(float v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double bd = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(orc_e4m3_value((unsigned)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) { best = c; bd = d; }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/*
+ * Per-token -> per-tensor requantisation of an expert-major FP8 payload.
+ *   x        uint8 E4M3 [E, max_m, K]
+ *   scale    fp32, entry (e, g, m) at e*se + g*sg + m*sm (g = k / group)
+ *   masked_m int32 [E]: valid rows of each expert (clamped to [0, max_m])
+ *   tensor_scale: S; out = e4m3((x * s) * (1 / S)) in fp32 steps
+ *   out      uint8 [E, max_m, K]; rows at or past masked_m are not written.
+ * Returns 0, or -1 on bad arguments.
+ */
+int orc_requant(const uint8_t* x, const float* scale, long se, long sg, long sm, const int32_t* masked_m,
+                int E, int max_m, int K, int group, float tensor_scale, uint8_t* out) {
+    if (E < 0 || max_m < 0 || K <= 0 || group <= 0 || K % group) return -1;
+    const float r = 1.0f / tensor_scale;
+    for (int e = 0; e < E; ++e) {
+        int rows = masked_m[e] < 0 ? 0 : (masked_m[e] > max_m ? max_m : masked_m[e]);
+        for (int m = 0; m < rows; ++m) {
+            const uint8_t* xr = x + ((long)e * max_m + m) * K;
+            uint8_t* orow = out + ((long)e * max_m + m) * K;
+            for (int k = 0; k < K; ++k) {
+                float s = scale[e * se + (long)(k / group) * sg + m * sm];
+                float t = (float)orc_e4m3_value(xr[k]);
+                t = t * s;
+                t = t * r;
+                orow[k] = orc_e4m3_encode(t);
+            }
+        }
+    }
     return 0;
 }

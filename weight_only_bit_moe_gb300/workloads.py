@@ -237,3 +237,60 @@ def make_batch(wl: Workload, M: int, seed: int) -> BatchInputs:
 def make_case(name: str, M: int, rep: int = 0):
     wl = WORKLOADS[name]
     return wl, make_weights(wl, weight_seed(name)), make_batch(wl, M, batch_seed(name, M, rep))
+
+
+# ---------------------------------------------------------------- W4AFP8 activation requantisation
+
+@dataclasses.dataclass(frozen=True)
+class RequantWorkload:
+    """An expert-major FP8 activation payload as a low-latency dispatcher hands it
+    to the W4AFP8 expert GEMM ("W4AFP8 requant ..." (sglang PR #35760)): E experts
+    of max_m row slots of K columns, masked_m valid rows each, one fp32 scale per
+    (row, 128-column group)."""
+    name: str
+    E: int
+    max_m: int
+    K: int
+    rows: str            # "one" (1 row per expert), "uniform", "skew" (one hot expert), "random"
+    mean_rows: int = 1
+    skew: int = 16       # "skew": the hot expert takes skew * mean_rows (capped at max_m)
+    group: int = 128
+
+
+REQUANT_WORKLOADS = {
+    # the page's decode case: 256 local experts, one row each, DeepSeek-V3 width
+    "requant-ll-1row": RequantWorkload("requant-ll-1row", E=256, max_m=128, K=7168, rows="one"),
+    # a loaded low-latency batch, evenly and unevenly routed
+    "requant-ll-uniform": RequantWorkload("requant-ll-uniform", E=32, max_m=512, K=7168, rows="uniform",
+                                          mean_rows=256),
+    "requant-ll-skew": RequantWorkload("requant-ll-skew", E=32, max_m=1024, K=7168, rows="skew", mean_rows=64),
+}
+
+
+@dataclasses.dataclass
+class RequantInputs:
+    x: np.ndarray         # uint8 E4M3 [E, max_m, K]
+    scale: np.ndarray     # fp32 [E, K/group, max_m] (group-major per expert, the dispatcher's layout)
+    masked_m: np.ndarray  # int32 [E]
+    tensor_scale: float   # S
+
+
+def make_requant(wl: RequantWorkload, seed: int) -> RequantInputs:
+    """Codes uniform over the finite E4M3 values, scales U[0.002, 0.02], S = 0.01 (so
+    that products span the format and some saturate), valid rows by wl.rows."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    codes = rng.integers(0, 254, size=(wl.E, wl.max_m, wl.K), dtype=np.int64)
+    codes = codes + (codes >= 0x7F)  # skip 0x7F (NaN); 0xFF is past the range
+    x = codes.astype(np.uint8)
+    scale = rng.uniform(0.002, 0.02, size=(wl.E, wl.K // wl.group, wl.max_m)).astype(np.float32)
+    if wl.rows == "one":
+        mm = np.ones(wl.E, dtype=np.int32)
+    elif wl.rows == "uniform":
+        mm = np.full(wl.E, wl.mean_rows, dtype=np.int32)
+    elif wl.rows == "skew":
+        mm = np.full(wl.E, wl.mean_rows, dtype=np.int32)
+        mm[int(rng.integers(0, wl.E))] = wl.skew * wl.mean_rows
+    else:
+        mm = rng.integers(0, wl.max_m + 1, size=wl.E).astype(np.int32)
+    mm = np.minimum(mm, wl.max_m).astype(np.int32)
+    return RequantInputs(x, scale, mm, 0.01)
