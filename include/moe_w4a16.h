@@ -104,9 +104,16 @@ typedef struct moe_layer_desc {
  *   w2     uint8 [E, K, N/2];  w2_s [E, K, N/g];  w2_gs fp32 [E] (NVFP4);
  *   b2     bf16 [E, K]          when has_bias2, else NULL
  *   packed device buffer of moe_repack_size() bytes, 256-byte aligned.
- * Returns MOE_ERR_INVALID for shapes outside the rules above, odd 2N rows
- * when interleaved (the ValueError cases of deinterleave_moe_mxfp4_w13_for_marlin)
- * or non_gated together with w13_interleaved. */
+ * Returns MOE_ERR_INVALID for shapes outside the rules above or non_gated
+ * together with w13_interleaved.  (The ValueError cases of
+ * deinterleave_moe_mxfp4_w13_for_marlin -- an odd row count, scale or bias rows
+ * not matching the weight rows -- cannot arise here: every row count derives
+ * from desc, 2N for interleaved banks.)
+ * Each expert matrix's scales are stored shifted by a power of two into the
+ * kernels' exact fp16 window, the shift undone by the expert's fp32 factor (see
+ * "Operand range" at moe_w4a16_forward); a matrix whose scales spread wider
+ * than the window marks the blob, and forwards on it report
+ * MOE_ERR_UNSUPPORTED through moe_get_status. */
 int64_t moe_repack_size(const moe_layer_desc* desc);
 int moe_repack_weights(const moe_layer_desc* desc, const void* w13, const void* w13_s,
                        const float* w13_gs, const void* b13, const void* w2, const void* w2_s,
@@ -156,20 +163,44 @@ int64_t moe_workspace_size(const moe_layer_desc* desc, int M, int top_k, int blo
  *            (_expert_norm_factors / _expert_norm_sum, weight_first)
  * Non-local pairs contribute nothing.  Arithmetic: fp32 accumulation, scales,
  * bias, activation and combine; the tensor-core operands are fp16 (weights
- * dequantised exactly, x and a rounded to fp16); a and y are kept as fp16
- * between the kernels (16-bit, as the Marlin path keeps its GEMM2 output); the
+ * dequantised exactly, x converted to fp16 -- exact inside its range -- and a
+ * rounded to fp16); a is kept as fp16 and y as fp32 between the kernels; the
  * combine sums in fp32 and writes out as bf16.
  * Arguments (device unless said): packed from moe_repack_weights for `desc`;
  * x bf16 [M, K]; topk_ids int32 [M, top_k]; topk_weights fp32 [M, top_k];
  * sorted_ids / expert_ids / n_padded from moe_align with the same M, top_k,
- * expert_base, E and block_m; act a moe_act (MOE_ACT_RELU2 exactly when
+ * expert_base, E and block_m -- or all three NULL: the forward then aligns the
+ * routing itself, in its first kernel, into the workspace (one launch fewer,
+ * the same result bit for bit); act a moe_act (MOE_ACT_RELU2 exactly when
  * desc->non_gated); alpha, limit (host) for
  * SIGMOID_ALPHA (limit = +inf: no clamp); post_norm_w bf16 [K] or NULL;
  * out bf16 [M, K]; workspace of at least moe_workspace_size() bytes.  packed and
  * workspace must be 256-byte aligned; x, out and post_norm_w 16-byte aligned.
- * Operand range: the tensor-core operands are 16-bit (fp16 for GEMM2 and for
- * INT4's GEMM1) and y is fp16, so inputs, activations and expert outputs must
- * stay inside the fp16 range (|v| < 65504); MXFP4 scales must lie in [2^-20, 2^9] (E8M0 bytes 107..136).
+ * E <= 1024 (the alignment's limit).
+ * Operand range: the tensor-core operands are fp16 and a is kept as fp16, so
+ * x and the activations a must stay inside the fp16 range (|v| < 65504; values
+ * below 2^-14 keep fewer significant bits).
+ * A value that leaves it (or is not a number) is not an argument error: the
+ * forward completes and records MOE_ERR_UNSUPPORTED for moe_get_status.
+ * Dequantised weights are exact fp16 operands for every scale within these
+ * windows, per expert and matrix (w13 or w2): the scales are shifted at repack
+ * by a power of two into the window and the expert's fp32 epilogue factor
+ * undoes the shift, so only the spread of one expert matrix's scales matters:
+ *   INT4:  largest / smallest nonzero |scale| below 2^26 (binary exponents
+ *          spanning at most 26 values);
+ *   MXFP4: E8M0 bytes spanning at most 37 values (largest - smallest <= 36);
+ *   NVFP4: any E4M3 scale.
+ * A wider spread keeps the largest scales exact and rounds the smallest blocks;
+ * moe_repack_weights marks the packed blob and every forward on it records
+ * MOE_ERR_UNSUPPORTED (INT4: only forwards with block_m >= 64, whose kernel
+ * dequantises with fp16 scales; the block_m <= 32 kernel applies INT4 scales
+ * in fp32).
+ * Alignment arguments: sorted_ids, expert_ids and n_padded are validated on the
+ * device as they are read -- n_padded outside [0, moe_align_capacity(M, top_k,
+ * E, block_m)] or not a multiple of block_m, an expert id outside [0, E), a
+ * sorted id outside [0, M*top_k) -- and never lead to an access outside the
+ * workspace, packed or out; such blocks and slots are skipped and
+ * moe_get_status reports MOE_ERR_INVALID afterwards.
  * M == 0 is a no-op. */
 int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void* x, int M,
                       int top_k, const int32_t* topk_ids, const float* topk_weights,
@@ -203,9 +234,14 @@ int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void
  * (cudaGetSymbolAddress, which can load the module) and the tensor-map
  * encoder; make one call on each device before any stream capture.  Nothing
  * is claimed about behaviour under capture.
- *   Status: a device wait that runs out of iterations is recorded in the
- * array's status word, which this entry point does not report; callers that
- * need that report use moe_w4a16_forward and moe_get_status. */
+ *   Status: device-side reports (a wait that runs out, a value outside the fp16
+ * operand range, inconsistent alignment inputs) are recorded in the array's
+ * status word, which this entry point does not report; callers that need them
+ * use moe_w4a16_forward and moe_get_status.  Decode-sized shapes may run with
+ * fewer K splits (down to none) than moe_w4a16_forward would choose.
+ *   Lifetime: the array's device address is looked up once per device and
+ * cached; the library must not be used across a reset of the device
+ * (cudaDeviceReset), after which the cached address is stale. */
 #define MOE_NOALLOC_SCRATCH_BYTES ((int64_t)64 << 20)
 int moe_w4a16_forward_noalloc(const moe_layer_desc* desc, const void* packed, const void* x,
                               int M, int top_k, const int32_t* topk_ids,
@@ -216,7 +252,11 @@ int moe_w4a16_forward_noalloc(const moe_layer_desc* desc, const void* packed, co
                               float norm_eps, void* out, void* stream);
 
 /* Synchronises `stream`, returns the device status recorded in `workspace` by
- * earlier forwards on it (MOE_OK or MOE_ERR_TIMEOUT) and clears it. */
+ * the last forward on it and clears it: MOE_OK; MOE_ERR_TIMEOUT (a device wait
+ * ran out); MOE_ERR_INVALID (alignment inputs inconsistent with the call);
+ * MOE_ERR_UNSUPPORTED (a value outside the fp16 operand range, see
+ * moe_w4a16_forward), in that order of precedence.  Each forward clears the word
+ * in its first kernel. */
 int moe_get_status(void* workspace, void* stream);
 
 /* Tracing hook.  With events != NULL and n == 4, every later moe_w4a16_forward

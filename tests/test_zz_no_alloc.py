@@ -44,6 +44,8 @@ def _run_both(wl, W, X, block_m=None):
                                     pnw, wl.norm_eps, out)
         outs.append(out)
     torch.cuda.synchronize()
+    # (the status read here is the workspace forward's: the allocation-free calls
+    # record theirs in the fixed array, which this entry point does not report)
     assert layer.status() == 0
     return ref.float().cpu().numpy(), [o.float().cpu().numpy() for o in outs]
 

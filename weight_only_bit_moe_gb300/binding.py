@@ -21,7 +21,8 @@ MOE_ACT_SILU_MUL, MOE_ACT_SIGMOID_ALPHA, MOE_ACT_RELU2 = 0, 1, 2
 
 EXPORTED = ("moe_repack_size", "moe_repack_weights", "moe_align_capacity", "moe_align", "moe_choose_block_m",
             "moe_workspace_size", "moe_w4a16_forward", "moe_w4a16_forward_noalloc", "moe_get_status",
-            "moe_set_trace_events", "moe_set_test_starve_wait", "moe_status_string")
+            "moe_set_trace_events", "moe_set_test_starve_wait", "moe_status_string", "moe_requant_fp8",
+            "moe_requant_launch_geometry")
 MOE_NOALLOC_SCRATCH_BYTES = 64 << 20  # fixed workspace of moe_w4a16_forward_noalloc
 
 
@@ -69,6 +70,9 @@ def load(path: str = ""):
                 "moe_set_trace_events": (i32, [ctypes.POINTER(ctypes.c_void_p), i32]),
                 "moe_set_test_starve_wait": (i32, [i32]),
                 "moe_status_string": (ctypes.c_char_p, [i32]),
+                "moe_requant_fp8": (i32, [p, p, i64, i64, i64, p, i32, i32, i32, i32, p, p, i32, p]),
+                "moe_requant_launch_geometry": (i32, [i32, i32, i32, i32, ctypes.POINTER(i32),
+                                                      ctypes.POINTER(i32)]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -190,3 +194,21 @@ def moe_set_trace_events(events) -> None:
 def moe_set_test_starve_wait(on: bool) -> None:
     """Test hook of the device failure path (see include/moe_w4a16.h)."""
     _check("moe_set_test_starve_wait", load().moe_set_test_starve_wait(1 if on else 0))
+
+
+def moe_requant_fp8(x, scale, scale_strides, masked_m, num_experts, max_m, K, group, tensor_scale, out,
+                    expected_rows=-1, stream=None):
+    """Per-token -> per-tensor FP8 requantisation (include/moe_requant.h).  scale_strides
+    = (e, g, m) element strides of the fp32 scale buffer."""
+    se, sg, sm = (int(v) for v in scale_strides)
+    return _check("moe_requant_fp8", load().moe_requant_fp8(
+        _p(x), _p(scale), se, sg, sm, _p(masked_m), num_experts, max_m, K, group, _p(tensor_scale), _p(out),
+        int(expected_rows), _stream(stream)))
+
+
+def moe_requant_launch_geometry(num_experts: int, K: int, expected_rows: int, sm_count: int):
+    """(ctas, threads) moe_requant_fp8 launches with (host only)."""
+    c, t = ctypes.c_int(0), ctypes.c_int(0)
+    _check("moe_requant_launch_geometry", load().moe_requant_launch_geometry(
+        num_experts, K, expected_rows, sm_count, ctypes.byref(c), ctypes.byref(t)))
+    return c.value, t.value

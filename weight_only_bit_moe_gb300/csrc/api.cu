@@ -12,7 +12,7 @@
 
 #include "combine.cuh"
 #include "gemm_launch.cuh"
-#include "prep.cuh"
+#include "prologue.cuh"
 
 namespace moe {
 
@@ -38,8 +38,8 @@ struct WsPlan {
   int64_t cap, blocks;
   int grid;
   int max_split1, max_split2, rows1, rows2;
-  int64_t status_off, counters1_off, counters2_off, header_bytes, xs_off, a_off, y_off, part1_off, part2_off,
-      total;
+  int64_t status_off, counters1_off, counters2_off, header_bytes, align_off, xh_off, a_off, y_off, part1_off,
+      part2_off, total;
 };
 
 bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
@@ -68,16 +68,23 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   off += (int64_t)L.T2 * w->blocks * 4;
   w->header_bytes = off;  // zeroed by the prologue every call
   off = round_up64(off, 256);
-  w->xs_off = off;  // routed rows in sorted order, 16-bit
-  off = round_up64(off + cap * L.K * 2, 256);
+  // the alignment, when the forward computes it: sorted [cap], experts [cap/B], n_padded, and each
+  // pair's sorted position [pairs]
+  w->align_off = off;
+  off = round_up64(off + (cap + w->blocks + 1 + pairs) * 4, 256);
+  // x as fp16: its own rows [M, K] for the register-fed kernels (block_m <= 32),
+  // the routed rows in sorted order [cap, K] for the tcgen05 kernels
+  w->xh_off = off;
+  off = round_up64(off + (block_m <= 32 ? (int64_t)M : cap) * L.K * 2, 256);
   w->a_off = off;
   off = round_up64(off + cap * L.Npad * 2, 256);
   w->y_off = off;
-  off = round_up64(off + pairs * L.K * 2, 256);  // y, fp16
+  off = round_up64(off + pairs * L.K * 4, 256);  // y, fp32
+  // (a GEMM that cannot split, max_split 1, never touches its partial area)
   w->part1_off = off;
-  off = round_up64(off + (int64_t)w->max_split1 * per1, 256);
+  off = round_up64(off + (w->max_split1 > 1 ? (int64_t)w->max_split1 * per1 : 0), 256);
   w->part2_off = off;
-  off = round_up64(off + (int64_t)w->max_split2 * per2, 256);
+  off = round_up64(off + (w->max_split2 > 1 ? (int64_t)w->max_split2 * per2 : 0), 256);
   w->total = off;
   return true;
 }
@@ -108,6 +115,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
   return fn;
+}
+
+// A row-major [rows, cols] fp16 matrix as a 2-D map with a one-row box of 64
+// columns and the 128-byte swizzle, for four-row TMA gathers.
+bool make_gather_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || cols % 64) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64u, 1u};
+  const cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // A row-major [rows, cols] fp16 matrix viewed as [rows][cols / 64][64]: dims (64, rows, cols / 64),
@@ -204,13 +225,16 @@ static int check_forward_args(const moe_layer_desc* desc, const void* packed, co
                               const void* post_norm_w, const void* out, Layout* L) {
   if (!desc || !make_layout(*desc, L)) return MOE_ERR_INVALID;
   if (M < 0 || top_k <= 0 || top_k > 16 || !valid_block_m(block_m)) return MOE_ERR_INVALID;
+  if (desc->num_experts > 1024) return MOE_ERR_INVALID;  // moe_align's limit: no alignment exists for more
   // gated experts take a gated activation, non-gated ones relu^2
   if (L->gated ? (act != MOE_ACT_SILU_MUL && act != MOE_ACT_SIGMOID_ALPHA) : act != MOE_ACT_RELU2)
     return MOE_ERR_INVALID;
   if ((int64_t)M * top_k >= (int64_t)1 << 31) return MOE_ERR_INVALID;
   if (M == 0) return MOE_OK;
-  if (!packed || !x || !topk_ids || !topk_weights || !sorted_ids || !expert_ids || !n_padded || !out)
-    return MOE_ERR_INVALID;
+  if (!packed || !x || !topk_ids || !topk_weights || !out) return MOE_ERR_INVALID;
+  // the alignment comes from moe_align (all three) or from the forward itself (none)
+  const int given = (sorted_ids != nullptr) + (expert_ids != nullptr) + (n_padded != nullptr);
+  if (given != 0 && given != 3) return MOE_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(packed) & 255) || (reinterpret_cast<uintptr_t>(x) & 15) ||
       (reinterpret_cast<uintptr_t>(out) & 15) || (reinterpret_cast<uintptr_t>(post_norm_w) & 15))
     return MOE_ERR_INVALID;
@@ -230,27 +254,72 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   const bool small = block_m <= kSmallBlockMax;
   const int bn = block_m;  // token columns per tile
 
-  GemmArgs g{};
-  // GEMM1 reads the gathered fp16 rows; GEMM2 GEMM1's fp16 output
-  CUtensorMap map2;
-  const int box_stages = small ? kSmallChunk : kSup;  // 64-K stages per activation copy
-  if (!make_act_map3(&g.tmap_b, ws + w.xs_off, L.K, w.cap, bn, box_stages)) return MOE_ERR_CUDA;
-  if (!make_act_map3(&map2, ws + w.a_off, L.Npad, w.cap, bn, box_stages)) return MOE_ERR_CUDA;
+  // The alignment: the caller's (from moe_align, two launches back by the time
+  // the GEMMs start) or computed here by the prologue into the workspace.
+  const bool own_align = sorted_ids == nullptr;
+  if (own_align) {
+    int32_t* base = reinterpret_cast<int32_t*>(ws + w.align_off);
+    sorted_ids = base;
+    expert_ids = base + w.cap;
+    n_padded = base + w.cap + w.blocks;
+  }
 
-  // prologue: status word and split-K counters to zero, routed rows gathered
-  PrepArgs pa{};
+  GemmArgs g{};
+  // GEMM1's activation rows: the register-fed kernel gathers x's rows (fp16) by
+  // token, the tcgen05 kernel reads them in sorted order; GEMM2 reads GEMM1's
+  // fp16 output in sorted order
+  CUtensorMap map2;
+  if (small ? !make_gather_map(&g.tmap_b, ws + w.xh_off, L.K, M)
+            : !make_act_map3(&g.tmap_b, ws + w.xh_off, L.K, w.cap, bn, kSup))
+    return MOE_ERR_CUDA;
+  if (!make_act_map3(&map2, ws + w.a_off, L.Npad, w.cap, bn, small ? kSmallChunk : kSup)) return MOE_ERR_CUDA;
+
+  // prologue: [alignment,] x to fp16 (rows or sorted order), status word and split-K counters to zero.
+  // Aligning in a launch of its own lets the GEMMs find the alignment two
+  // launches back and stream weights while the prologue runs, which is worth
+  // more than one launch less for decode-sized blocks and for short batches
+  // (measured on GB300).  Large batches on the tcgen05 path align and place
+  // x's routed rows in one launch (no second pass over the sorted slots).
+  const bool split_align = own_align && (small || (int64_t)M * top_k * L.K < ((int64_t)1 << 25));
+  PrologueArgs pa{};
+  pa.pairs = M * top_k;
+  pa.cap = w.cap;
+  if (split_align) {
+    PrologueArgs al{};
+    al.topk_ids = topk_ids;
+    al.pairs = M * top_k;
+    al.expert_base = expert_base;
+    al.E = L.E;
+    al.block_m = block_m;
+    al.cap = w.cap;
+    al.sorted_ids = const_cast<int32_t*>(sorted_ids);
+    al.expert_ids = const_cast<int32_t*>(expert_ids);
+    al.n_padded = const_cast<int32_t*>(n_padded);
+    if (launch_prologue(al, 0, st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (own_align && !split_align) {
+    pa.topk_ids = topk_ids;
+    pa.expert_base = expert_base;
+    pa.E = L.E;
+    pa.block_m = block_m;
+    pa.sorted_ids = const_cast<int32_t*>(sorted_ids);
+    pa.expert_ids = const_cast<int32_t*>(expert_ids);
+    pa.n_padded = const_cast<int32_t*>(n_padded);
+    pa.pair_pos = const_cast<int32_t*>(n_padded) + 1;
+    if (!small) pa.align_ctas = align_copy_ctas(M * top_k, L.K, w.grid);
+  } else {
+    pa.given_sorted = sorted_ids;
+    pa.given_n_padded = n_padded;
+  }
+  pa.x = static_cast<const uint16_t*>(x);
+  pa.M = M;
+  pa.K = L.K;
+  pa.top_k = top_k;
+  if (small) pa.xh = reinterpret_cast<uint16_t*>(ws + w.xh_off);
+  else pa.xs = reinterpret_cast<uint16_t*>(ws + w.xh_off);
   pa.zero = reinterpret_cast<uint32_t*>(ws);
   pa.zero_words = w.header_bytes / 4;
-  pa.x = static_cast<const uint16_t*>(x);
-  pa.xs = reinterpret_cast<uint16_t*>(ws + w.xs_off);
-  pa.sorted_ids = sorted_ids;
-  pa.n_padded = n_padded;
-  pa.cap = w.cap;
-  pa.pairs = M * top_k;
-  pa.top_k = top_k;
-  pa.K = L.K;
-  pa.to_f16 = 1;
-  if (launch_prep(pa, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_prologue(pa, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (trace(0, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   g.L = L;
@@ -258,13 +327,16 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.sorted_ids = sorted_ids;
   g.expert_ids = expert_ids;
   g.n_padded = n_padded;
+  g.cap = w.cap;
   g.pairs = M * top_k;
+  g.top_k = top_k;
+  g.align_early = (own_align && !split_align) ? 0 : 1;
   g.block_m = block_m;
   g.act_kind = act;
   g.alpha = alpha;
   g.limit = limit;
   g.a_out = reinterpret_cast<uint16_t*>(ws + w.a_off);
-  g.y_out = reinterpret_cast<uint16_t*>(ws + w.y_off);
+  g.y_out = reinterpret_cast<float*>(ws + w.y_off);
   g.status = reinterpret_cast<unsigned*>(ws + w.status_off);
   g.test_starve_wait = g_test_starve_wait.load(std::memory_order_relaxed);
 
@@ -297,7 +369,7 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   c.E = L.E;
   c.topk_ids = topk_ids;
   c.topk_weights = topk_weights;
-  c.y = reinterpret_cast<const uint16_t*>(ws + w.y_off);
+  c.y = reinterpret_cast<const float*>(ws + w.y_off);
   c.post_norm_w = static_cast<const uint16_t*>(post_norm_w);
   c.norm_eps = norm_eps;
   c.rsf = routed_scaling_factor;
@@ -403,6 +475,8 @@ extern "C" int moe_get_status(void* workspace, void* stream) {
   if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
   if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
+  if (v & kStatusRouting) return MOE_ERR_INVALID;
+  if (v & kStatusRange) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 

@@ -10,10 +10,11 @@
 //              _expert_norm_sum, weight_first, eps 1e-8; non-local slots get
 //              factor 0).
 //
-// y is fp16 (a 16-bit GEMM2 output, as the pages' Marlin path keeps it, with
-// fp16's 11 significant bits), summed in fp32.  Each thread owns 8 consecutive columns (one
-// 16-byte load per slot, one 16-byte bf16 store) and issues every slot's loads
-// before it sums, in slot order.  Plain rows spread a token over a 2-D grid of 128-thread
+// y is fp32 (the expert outputs keep their accumulation precision: the top-k
+// sum can cancel terms of a few hundred down to a fraction of one), summed in
+// fp32.  Each thread owns 8 consecutive columns (two 16-byte loads per slot,
+// one 16-byte bf16 store) and issues every slot's loads before it sums, in
+// slot order.  Plain rows spread a token over a 2-D grid of 128-thread
 // column blocks; post-norm rows take one CTA per token, wide enough to cover
 // the row in one pass (up to 1024 threads), so the row reduction stays in it.
 #include <cuda_runtime.h>
@@ -36,16 +37,12 @@ __device__ __forceinline__ void bf16x8(const uint16_t* p, float (&v)[8]) {  // 8
   }
 }
 
-// y of one pair at columns [col, col+8).
+// y of one pair at columns [col, col+8) (two 16-byte loads).
 __device__ __forceinline__ void pair_y8(const CombineArgs& c, int pair, int col, float (&v)[8]) {
-  const uint4 u = __ldcg(reinterpret_cast<const uint4*>(c.y + (int64_t)pair * c.K + col));
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    v[2 * i] = f.x;
-    v[2 * i + 1] = f.y;
-  }
+  const float4* p = reinterpret_cast<const float4*>(c.y + (int64_t)pair * c.K + col);
+  const float4 a = __ldcg(p), b = __ldcg(p + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 __device__ __forceinline__ void norm_w8(const uint16_t* w, int col, float (&v)[8]) {

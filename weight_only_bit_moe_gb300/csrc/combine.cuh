@@ -9,7 +9,7 @@ struct CombineArgs {
   int M, top_k, K, expert_base, E;
   const int32_t* topk_ids;      // [M, top_k]
   const float* topk_weights;    // [M, top_k]
-  const uint16_t* y;            // GEMM2 output, fp16 [pairs, K] (rows of local pairs)
+  const float* y;               // GEMM2 output, fp32 [pairs, K] (rows of local pairs)
   const uint16_t* post_norm_w;  // [K] or NULL
   float norm_eps, rsf;
   uint16_t* out;                // [M, K]

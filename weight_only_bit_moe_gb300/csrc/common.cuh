@@ -65,7 +65,7 @@ struct Layout {
   int scale_bytes; // scale bytes per chunk
   int64_t period_bytes;   // scale_bytes + period * 8192
   int64_t tile1_bytes, tile2_bytes;
-  int64_t w13_off, w2_off, b13_off, b2_off, gs13_off, gs2_off, total;
+  int64_t w13_off, w2_off, b13_off, b2_off, gs13_off, gs2_off, shift_off, total;
 };
 
 __host__ __device__ inline int64_t round_up64(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
@@ -108,6 +108,8 @@ __host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
   off += (int64_t)L->E * 4;
   L->gs2_off = off = round_up64(off, 256);
   off += (int64_t)L->E * 4;
+  L->shift_off = off = round_up64(off, 256);  // int32 [2][E]: scale exponent shift of w13 and w2
+  off += (int64_t)2 * L->E * 4;
   L->total = round_up64(off, 256);
   return true;
 }
@@ -138,9 +140,34 @@ struct PackedFmt {
 constexpr float kFp4Unscale = 256.0f;
 
 // ----------------------------------------------------------------------------
+// Operand windows of the 16-bit tensor-core path and the per-expert scale shift.
+//
+// Dequantised weights are fp16 tensor-core operands and must be exact there.
+// INT4 (q - 8) * s with a bf16 scale s in [2^e, 2^(e+1)) is exact for
+// -13 <= e <= 12 (s / 16, used for the odd nibble pairs, keeps its 8
+// significant bits above fp16's 2^-24 quantum, and 8 s < 65504).  An MXFP4
+// weight e2m1 * 2^(b - 127), produced as e2m1 * 2^(b - 135), is exact for E8M0
+// bytes 112 <= b <= 148 (half of 2^(b - 135) stays on the 2^-24 grid, 6 of it
+// below 65504).  NVFP4 weights are exact for every E4M3 scale.  Each expert's
+// scales of one matrix are multiplied at repack by a power of two 2^d chosen so
+// that they fall into the window (d = 0 when they already do), and the epilogue
+// factor of that expert carries 2^-d, so the product is unchanged.  When the
+// scales of one expert matrix span more than the window, d keeps the largest
+// exact and the packed blob's header records the loss.
+// ----------------------------------------------------------------------------
+constexpr int kInt4ExpMin = -13, kInt4ExpMax = 12;
+constexpr int kE8m0Min = 112, kE8m0Max = 148;
+
+// Packed-blob header (its first 256 bytes): word 0 holds these flags.
+constexpr uint32_t kFlagInt4Window = 1u;  // an INT4 scale outside the fp16 window (tcgen05 path only)
+constexpr uint32_t kFlagFp4Window = 2u;   // an MXFP4 scale byte outside the fp16 window (both GEMM paths)
+
+// ----------------------------------------------------------------------------
 // Device status word (first 4 bytes of the forward workspace).
 // ----------------------------------------------------------------------------
-constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusTimeout = 1u;   // a bounded wait ran out
+constexpr unsigned kStatusRange = 2u;     // a value left the 16-bit operand range (see above)
+constexpr unsigned kStatusRouting = 4u;   // alignment inputs inconsistent with this layer
 
 // ----------------------------------------------------------------------------
 // PTX wrappers.
@@ -198,8 +225,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
+      // the predecessor kernel clears the status word: record after it completed
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       atomicOr(status, kStatusTimeout);
       return false;
+    }
+  }
+}
+
+// End-of-role drain: wait (at most kDrainLimitNs) for the phase with the given
+// parity, so that no copy or MMA is in flight when the CTA exits or frees
+// tensor memory; a drain that runs out records kStatusTimeout.
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, unsigned* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kDrainLimitNs) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      atomicOr(status, kStatusTimeout);
+      return;
     }
   }
 }
@@ -402,6 +446,19 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
                : "memory");
 }
 
+// max / min that propagate NaN (a running max over stored values then also
+// catches NaN, and a clamp keeps a NaN input NaN, as torch's clamp does).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
 // ---------------------------------------------------------------- bf16 bits
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
@@ -462,8 +519,10 @@ __device__ __forceinline__ uint32_t bf16_scale_f16(uint32_t sbits) {
   return __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
 }
 // E8M0 byte b -> 2^(b-127) * 2^-8 = 2^(b-135) as fp16 (normal for b >= 121,
-// subnormal power of two for 111 <= b <= 120).
+// subnormal power of two for 111 <= b <= 120, 0 below; 255 is NaN).  Bytes
+// above 150 do not occur: the repack shift keeps them in [112, 148].
 __device__ __forceinline__ uint32_t e8m0_mult_f16(uint32_t b) {
+  if (b == 255u) return 0x7E00u;
   return b >= 121u ? (((b - 120u) & 0x1Fu) << 10) : (b >= 111u ? (1u << (b - 111u)) : 0u);
 }
 // Two E4M3 bytes (low = first) -> f16x2 of value * 2^-8 (exact).

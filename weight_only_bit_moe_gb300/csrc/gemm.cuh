@@ -58,13 +58,20 @@ constexpr uint32_t kAColsPerStage = 64;                     // 2 halves x 64 K /
 constexpr uint32_t kAColsPerUnit = kSup * kAColsPerStage;
 
 struct GemmArgs {
-  CUtensorMap tmap_b;         // activation rows [rows, Kred] 16-bit as 3-D boxes of 64 x BN x stages
+  CUtensorMap tmap_b;         // activation rows: tcgen05 kernel, sorted order [cap, Kred] fp16 as 3-D
+                              // boxes of 64 x BN x stages (GEMM1: the prologue's xs, GEMM2: a);
+                              // register-fed GEMM1: x's rows [M, K] fp16 for 4-row gathers of 64
+                              // columns; register-fed GEMM2: a as 3-D boxes
   Layout L;
   const uint8_t* packed;      // repacked blob
   const int32_t* sorted_ids;
   const int32_t* expert_ids;
   const int32_t* n_padded;
+  int64_t cap;                // sorted slots the workspace holds (n_padded beyond it is an error)
   int pairs;                  // M * top_k (sentinel value)
+  int top_k;                  // token of a pair = pair / top_k (GEMM1's row gather)
+  int align_early;            // 1: the alignment was written two launches back (moe_align), so it may
+                              // be read before the dependency wait; 0: the prologue just wrote it
   int block_m;
   int has_bias;
   int act_kind;               // moe_act
@@ -72,7 +79,7 @@ struct GemmArgs {
   int max_split;
   int split_rows;             // rows of each split-K partial slice
   uint16_t* a_out;            // GEMM1 output, fp16 [cap, Npad]
-  uint16_t* y_out;            // GEMM2 output, fp16 [pairs, K]
+  float* y_out;               // GEMM2 output, fp32 [pairs, K]
   float* partial;             // split-K partials [max_split][split_rows][width]
   int32_t* counters;          // split-K arrival counters [T * blocks]
   unsigned* status;
@@ -115,8 +122,8 @@ __device__ __forceinline__ float act_fn(int kind, float g, float u, float alpha,
     const float hg = 0.5f * g;
     return fmaf(hg, tanh_approx(hg), hg) * u;  // g * sigmoid(g) * u
   }
-  const float gc = fminf(g, limit);
-  const float uc = fminf(fmaxf(u, -limit), limit);
+  const float gc = fmin_nan(g, limit);  // clamp(max=limit), NaN stays NaN
+  const float uc = fmin_nan(fmax_nan(u, -limit), limit);
   const float hg = 0.5f * gc;
   return fmaf(hg, tanh_approx(alpha * hg), hg) * (uc + 1.0f);  // gc * sigmoid(alpha * gc) * (uc + 1)
 }
@@ -147,6 +154,26 @@ __device__ __forceinline__ uint4 transpose8x8_u16(const uint32_t (&w)[4], int la
   return b2 ? make_uint4(rc, rd, x10, x11) : make_uint4(x00, x01, rc, rd);
 }
 
+// The same transpose for 32-bit values: on entry lane L holds feature L's
+// values of tokens 0..7 in v[0..7]; on exit v[j] holds feature (L & ~7) + j of
+// token L & 7.  Three butterfly steps (lane bit i <-> register bit i), four
+// shuffles each.
+__device__ __forceinline__ void transpose8x8_u32(float (&v)[8], int lane) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const int m = 1 << i;
+    const bool up = (lane >> i) & 1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j & m) continue;
+      const float send = up ? v[j] : v[j | m];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+      if (up) v[j] = recv;
+      else v[j | m] = recv;
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
@@ -163,9 +190,52 @@ struct WorkPlan {
   int items;
 };
 
+// Token blocks to run: n_padded / block_m, limited to the capacity the
+// workspace was planned for.  An n_padded outside [0, cap] or off the block
+// grid means the alignment came from other arguments: the clamp keeps every
+// access inside the workspace and routing_check() reports it.
+__device__ __forceinline__ int valid_blocks(const GemmArgs& g) {
+  const int np = *g.n_padded;
+  return (int)(min((int64_t)max(np, 0), g.cap) / g.block_m);
+}
+__device__ __forceinline__ bool routing_bad(const GemmArgs& g) {
+  const int np = *g.n_padded;
+  return np < 0 || (int64_t)np > g.cap || np % g.block_m != 0;
+}
+// The local expert of token block b, or -1 when the alignment names none of this
+// layer's experts (the block is then skipped by every role alike).
+__device__ __forceinline__ int block_expert(const GemmArgs& g, int b) {
+  const int e = g.expert_ids[b];
+  return (unsigned)e < (unsigned)g.L.E ? e : -1;
+}
+
+// A sorted slot holds a routed pair when its id is in [0, pairs) (the sentinel
+// pairs marks padding; anything else is treated as padding too).
+__device__ __forceinline__ bool live_sid(int sid, int pairs) { return (unsigned)sid < (unsigned)pairs; }
+
+// Header flags of the packed blob that make a kernel's fp16 operands inexact:
+// the tcgen05 path dequantises INT4 with fp16 scales, the register-fed path
+// applies INT4 scales in fp32; both turn MXFP4 scales into fp16 multipliers.
+constexpr uint32_t kStatusBlobFlagsTc = kFlagInt4Window | kFlagFp4Window;
+constexpr uint32_t kStatusBlobFlagsSmall = kFlagFp4Window;
+
+// End-of-kernel status of one epilogue thread (after its dependency wait): an
+// fp16 value that overflowed (|v| >= 65520 rounds to infinity) or is not a
+// number -- an activation that left the fp16 range makes GEMM1's sums
+// infinite or NaN, so this also reports inputs outside it -- and (one thread
+// of CTA 0) the blob's window flags and an inconsistent alignment.
+__device__ __forceinline__ void report_epilogue_status(const GemmArgs& g, float vmax, bool reporter,
+                                                       uint32_t blob_flags) {
+  if (!(vmax < 65520.0f)) atomicOr(g.status, kStatusRange);
+  if (reporter && blockIdx.x == 0) {
+    if (*reinterpret_cast<const uint32_t*>(g.packed) & blob_flags) atomicOr(g.status, kStatusRange);
+    if (routing_bad(g)) atomicOr(g.status, kStatusRouting);
+  }
+}
+
 __device__ __forceinline__ WorkPlan make_plan(const GemmArgs& g, bool gemm1) {
   WorkPlan p;
-  p.nb = *g.n_padded / g.block_m;
+  p.nb = valid_blocks(g);
   p.T = gemm1 ? g.L.T1 : g.L.T2;
   const int stages = gemm1 ? g.L.S1 : g.L.S2;
   p.units = stages / g.L.period;
@@ -213,6 +283,28 @@ __device__ __forceinline__ void tma_tile3d(uint32_t dst, const CUtensorMap* map,
       "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
+}
+
+// TMA gather: four rows (r[0..3]) of a 2-D row-major tensor, 64 fp16 columns
+// from c0 (the map's one-row box), land as four consecutive 128-byte rows at
+// dst with the map's 128-byte swizzle (applied by shared address, so a 512-byte
+// aligned dst continues the 1024-byte swizzle atom it sits in).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, const int4& r,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Token rows of block b's slots (padding slots read token 0; their columns are
+// discarded) into rows[0, n), by the n first lanes of the calling warp.
+__device__ __forceinline__ void load_block_rows(const GemmArgs& g, int b, int n, int lane, int32_t* rows) {
+  for (int i = lane; i < n; i += 32) {
+    const int sid = g.sorted_ids[b * g.block_m + i];
+    rows[i] = (unsigned)sid < (unsigned)g.pairs ? sid / g.top_k : 0;
+  }
 }
 
 template <int FMT, int STAGE, int BN>
@@ -264,12 +356,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   // Ordering against the stream predecessors (programmatic launch): this kernel
-  // starts only once its predecessor has passed its own wait, so the alignment
-  // outputs (n_padded, expert_ids, sorted_ids, written two launches earlier) and
-  // the packed weights are complete; the weight producer, the dequant warps and
-  // the MMA warp need no wait.  The activation producer and the epilogue, which
-  // read the predecessor's rows or write counters and outputs, wait first.
+  // starts only once its predecessor has passed its own wait.  When the
+  // alignment came from moe_align (align_early), it was written two launches
+  // back and is complete, with the packed weights, so the weight producer, the
+  // dequant warps and the MMA warp need no wait; the activation producer and the
+  // epilogue, which read the predecessor's rows or write counters and outputs,
+  // wait first.  When the prologue wrote the alignment, everyone waits.
   grid_dependents_launch();
+  if (!g.align_early) grid_dependency_wait();
 
   const WorkPlan plan = make_plan(g, kG1);
   const int64_t tile_bytes = kG1 ? L.tile1_bytes : L.tile2_bytes;
@@ -284,7 +378,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         int b, tile, split, s0, s1;
         decode_item(plan, w, b, tile, split);
         stage_range(plan, L, split, s0, s1);
-        const int e = g.expert_ids[b];
+        const int e = block_expert(g, b);
+        if (e < 0) continue;
         const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
         for (int s = s0; s < s1; s += kSup, ++pk) {
           const int slot = pk % kSP;
@@ -300,13 +395,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       // leave no copy in flight: wait for the last phase of every used slot
       for (uint32_t i = 0; i < (uint32_t)kSP && i < pk; ++i) {
         const uint32_t k = pk - 1 - i;
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&p_full[k % kSP], (k / kSP) & 1) && global_timer_ns() - t0 < 100000000ull) {
-        }
+        mbar_drain(&p_full[k % kSP], (k / kSP) & 1, g.status);
       }
     }
   } else if (warp == kWarpBProducer) {
     // ------------------------------------------------------------ TMA producer (activation rows)
+    // the block's rows in sorted order -- GEMM1: x's routed rows, which the
+    // prologue placed in sorted order; GEMM2: GEMM1's output -- one 3-D box per
+    // unit brings both of its stages (past K it reads zeros)
     if (lane == 0) {
       grid_dependency_wait();
       uint32_t bk = 0;
@@ -314,19 +410,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         int b, tile, split, s0, s1;
         decode_item(plan, w, b, tile, split);
         stage_range(plan, L, split, s0, s1);
+        if (block_expert(g, b) < 0) continue;
         for (int s = s0; s < s1; s += kSup, ++bk) {
           const int bs = bk % kSB;
           mbar_wait(&b_empty[bs], ((bk / kSB) + 1) & 1, abort_flag, g.status);
-          // one 3-D box brings both stages of the unit (past K it reads zeros)
           mbar_arrive_expect_tx(&b_full[bs], SM::kBUnitBytes);
           tma_tile3d(smem_u32(smem + SM::kB + bs * SM::kBUnitBytes), &g.tmap_b, 0, b * g.block_m, s, &b_full[bs]);
         }
       }
       for (uint32_t i = 0; i < (uint32_t)kSB && i < bk; ++i) {
         const uint32_t k = bk - 1 - i;
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&b_full[k % kSB], (k / kSB) & 1) && global_timer_ns() - t0 < 100000000ull) {
-        }
+        mbar_drain(&b_full[k % kSB], (k / kSB) & 1, g.status);
       }
     }
   } else if (warp == kWarpMma) {
@@ -337,10 +431,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     constexpr uint32_t idesc = idesc_f16_f32(128, BN, 0u);
     uint32_t ak = 0, bk = 0, ic = 0;
     const uint32_t b0 = smem_u32(smem + SM::kB);
-    for (int w = blockIdx.x; w < plan.items; w += gridDim.x, ++ic) {
+    for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
       int b, tile, split, s0, s1;
       decode_item(plan, w, b, tile, split);
       stage_range(plan, L, split, s0, s1);
+      if (block_expert(g, b) < 0) continue;  // (every role skips it; no counter moves)
       const int accb = ic % kNacc;
       mbar_wait(&acc_empty[accb], ((ic / kNacc) + 1) & 1, abort_flag, g.status);
       __syncwarp();
@@ -366,12 +461,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         umma_commit_elect(&b_empty[bs]);
       }
       umma_commit_elect(&acc_full[accb]);
+      ++ic;
     }
     // all issued MMAs complete before TMEM is released
     umma_commit_elect(drain_bar);
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < 100000000ull) {
-    }
+    mbar_drain(drain_bar, 0, g.status);
     __syncwarp();
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant warps
@@ -386,6 +480,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       int b, tile, split, s0, s1;
       decode_item(plan, w, b, tile, split);
       stage_range(plan, L, split, s0, s1);
+      if (block_expert(g, b) < 0) continue;
       for (int s = s0; s < s1; s += kSup, ++pk, ++ak) {
         const int ps = pk % kSP, as = ak % kSA;
         const int nst = min(kSup, s1 - s);
@@ -474,15 +569,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     const int width = kGated ? 2 * Npad : (kG1 ? Npad : L.K);  // partial row width
     const int bias_stride = kGated ? 2 * Npad : (kG1 ? Npad : L.Kpad2);
     uint32_t ic = 0;
-    for (int w = blockIdx.x; w < plan.items; w += gridDim.x, ++ic) {
+    float vmax = 0.0f;  // largest |value| stored as fp16 (NaN ignored)
+    for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
       int b, tile, split;
       decode_item(plan, w, b, tile, split);
+      const int e = block_expert(g, b);
+      if (e < 0) {  // a block inside n_padded without one of this layer's experts
+        if (et == 0 && split == 0) atomicOr(g.status, kStatusRouting);
+        continue;
+      }
       // everything the item's epilogue reads from global memory is fetched before
       // the accumulator wait, off the critical path
       const int jmax = min(BN, g.block_m);
       named_bar_sync(2, kEpiThreads);  // the previous item's readers of epi_sid are done
-      if (et < jmax) epi_sid[et] = g.sorted_ids[b * g.block_m + et];
-      const int e = g.expert_ids[b];
+      if (et < jmax) {
+        const int v = g.sorted_ids[b * g.block_m + et];
+        epi_sid[et] = v;
+        if ((unsigned)v > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);  // neither a pair nor padding
+      }
       const float gsc = gs_tab[e];
       // feature / output rows held by this thread in half 0 and half 1; for
       // gated GEMM1 both halves hold the same feature (gate and up)
@@ -587,8 +691,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             // consecutive features of one token (16 bytes)
             uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              w[j] = pack_f16x2(sid[2 * j] < g.pairs ? av[2 * j] : 0.0f, sid[2 * j + 1] < g.pairs ? av[2 * j + 1] : 0.0f);
+            for (int j = 0; j < 4; ++j) {
+              const float lo = live_sid(sid[2 * j], g.pairs) ? av[2 * j] : 0.0f;
+              const float hi = live_sid(sid[2 * j + 1], g.pairs) ? av[2 * j + 1] : 0.0f;
+              vmax = fmax_nan(vmax, fmax_nan(fabsf(lo), fabsf(hi)));
+              w[j] = pack_f16x2(lo, hi);
+            }
             const uint4 o = transpose8x8_u16(w, lane);
             const int tt = lane & 7;
             if (c0 + tt < jmax) stg128(g.a_out + (int64_t)(pos0 + tt) * Npad + (row0 - hr) + q * 32 + (lane & 24), o);
@@ -596,9 +704,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             uint32_t w0[4], w1[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const bool l0 = sid[2 * j] < g.pairs, l1 = sid[2 * j + 1] < g.pairs;
-              w0[j] = pack_f16x2(l0 ? relu2(f0[2 * j] * gsc + bias0) : 0.0f, l1 ? relu2(f0[2 * j + 1] * gsc + bias0) : 0.0f);
-              w1[j] = pack_f16x2(l0 ? relu2(f1[2 * j] * gsc + bias1) : 0.0f, l1 ? relu2(f1[2 * j + 1] * gsc + bias1) : 0.0f);
+              const bool l0 = live_sid(sid[2 * j], g.pairs), l1 = live_sid(sid[2 * j + 1], g.pairs);
+              const float h00 = f0[2 * j] * gsc + bias0, h01 = f0[2 * j + 1] * gsc + bias0;
+              const float h10 = f1[2 * j] * gsc + bias1, h11 = f1[2 * j + 1] * gsc + bias1;
+              const float a00 = l0 ? relu2(h00) : 0.0f, a01 = l1 ? relu2(h01) : 0.0f;
+              const float a10 = l0 ? relu2(h10) : 0.0f, a11 = l1 ? relu2(h11) : 0.0f;
+              // relu^2 >= 0; h * 0 is NaN exactly when h is not finite (relu2 maps NaN to 0)
+              vmax = fmax_nan(vmax, fmax_nan(fmax_nan(a00, a01), fmax_nan(a10, a11)));
+              vmax = fmax_nan(vmax, (l0 ? (h00 + h10) * 0.0f : 0.0f) + (l1 ? (h01 + h11) * 0.0f : 0.0f));
+              w0[j] = pack_f16x2(a00, a01);
+              w1[j] = pack_f16x2(a10, a11);
             }
             const uint4 o0 = transpose8x8_u16(w0, lane), o1 = transpose8x8_u16(w1, lane);
             const int tt = lane & 7;
@@ -608,32 +723,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               stg128(dst + 128, o1);
             }
           } else {
-            // fp16 rows by pair, transposed like GEMM1's: each lane stores 8
-            // consecutive outputs of one pair per half; ok0/ok1 are warp-uniform
-            // (K % 64 == 0 and a warp's 32 rows start on a multiple of 32)
+            // fp32 rows by pair, transposed: each lane stores 8 consecutive
+            // outputs of one pair per half (two 16-byte stores); ok0/ok1 are
+            // warp-uniform (K % 64 == 0 and a warp's 32 rows start on a multiple
+            // of 32).  Padding columns are stored by no lane.
             const int tt = lane & 7;
             const int sid_t = epi_sid[c0 + tt];
-            const bool live = c0 + tt < jmax && sid_t < g.pairs;
-            uint16_t* dst = g.y_out + (int64_t)(live ? sid_t : 0) * L.K + (row0 - hr) + q * 32 + (lane & 24);
-            uint32_t w[4];
+            const bool live = c0 + tt < jmax && live_sid(sid_t, g.pairs);
+            float* dst = g.y_out + (int64_t)(live ? sid_t : 0) * L.K + (row0 - hr) + q * 32 + (lane & 24);
+            // y is fp32: only a non-finite value of a live column is an error
+            // (NaN, or an infinity from an overflow upstream)
             if (ok0) {
+              float v[8];
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                w[j] = pack_f16x2(f0[2 * j] * gsc + bias0, f0[2 * j + 1] * gsc + bias0);
-              const uint4 o = transpose8x8_u16(w, lane);
-              if (live) stg128(dst, o);
+              for (int j = 0; j < 8; ++j) {
+                v[j] = f0[j] * gsc + bias0;
+                if (live_sid(sid[j], g.pairs)) vmax = fmax_nan(vmax, v[j] * 0.0f);
+              }
+              transpose8x8_u32(v, lane);
+              if (live) {
+                stg128(dst, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3])));
+                stg128(dst + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]), __float_as_uint(v[7])));
+              }
             }
             if (ok1) {
+              float v[8];
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                w[j] = pack_f16x2(f1[2 * j] * gsc + bias1, f1[2 * j + 1] * gsc + bias1);
-              const uint4 o = transpose8x8_u16(w, lane);
-              if (live) stg128(dst + 128, o);
+              for (int j = 0; j < 8; ++j) {
+                v[j] = f1[j] * gsc + bias1;
+                if (live_sid(sid[j], g.pairs)) vmax = fmax_nan(vmax, v[j] * 0.0f);
+              }
+              transpose8x8_u32(v, lane);
+              if (live) {
+                stg128(dst + 128, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3])));
+                stg128(dst + 132, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]), __float_as_uint(v[7])));
+              }
             }
           }
         }
       }
+      ++ic;
     }
+    report_epilogue_status(g, vmax, et == 0, kStatusBlobFlagsTc);
   }
 
   tc_fence_before();

@@ -48,7 +48,8 @@ struct SmallSmem {
   static constexpr int kSlots = kFit > 6 ? 6 : kFit;
   static constexpr int kBar = kSlots * kSlotBytes;
   static constexpr int kMisc = kBar + 2 * kSlots * 8;
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kRows = kMisc + 64;  // GEMM1 token rows: the current item's, then one set per slot
+  static constexpr int kBytes = kRows + (1 + kSlots) * 32 * 4;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kSlots >= 4, "ring too shallow");
   static_assert(kAlloc <= 232448, "shared memory over the per-CTA limit");
@@ -60,7 +61,7 @@ struct SmallSmem {
 // = BN/8 stages) and the last CTA of each item reads S of them back.
 __device__ __forceinline__ WorkPlan make_plan_small(const GemmArgs& g, bool gemm1, int bn) {
   WorkPlan p;
-  p.nb = *g.n_padded / g.block_m;
+  p.nb = valid_blocks(g);
   p.T = gemm1 ? g.L.T1 : g.L.T2;
   const int stages = gemm1 ? g.L.S1 : g.L.S2;
   p.units = stages / g.L.period;
@@ -266,12 +267,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&g.tmap_b)) : "memory");
   __syncthreads();
   // Ordering against the stream predecessors (programmatic launch): this kernel
-  // starts only once its predecessor has passed its own wait, so the alignment
-  // outputs (n_padded, expert_ids, sorted_ids, written two launches earlier) and
-  // the packed weights are complete and the producer streams weights at once.
-  // The activation rows, the split-K counters and the outputs belong to the
-  // predecessor: every thread that touches them waits first.
+  // starts only once its predecessor has passed its own wait.  When the
+  // alignment came from moe_align (align_early), it was written two launches
+  // back and is complete, with the packed weights, so the producer streams
+  // weights at once; the activation rows, the split-K counters and the outputs
+  // belong to the predecessor, and every thread that touches them waits first.
+  // When the prologue wrote the alignment, everyone waits.
   grid_dependents_launch();
+  if (!g.align_early) grid_dependency_wait();
 
   const WorkPlan plan = make_plan_small(g, kG1, BN);
   const int64_t tile_bytes = kG1 ? L.tile1_bytes : L.tile2_bytes;
@@ -279,59 +282,87 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      // The first ring's worth of weight copies go out before the wait on the
-      // predecessor; their activation boxes (the predecessor's output) follow it.
-      // Each slot's barrier expects both byte counts from the start.
-      int pend_row[kSlots], pend_stage[kSlots];
-      uint32_t npend = 0;
-      bool waited = false;
-      uint32_t ck = 0;
-      for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
-        int b, tile, split, s0, s1;
-        decode_item(plan, w, b, tile, split);
-        stage_range(plan, L, split, s0, s1);
-        const int e = g.expert_ids[b];
-        const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
-        for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
-          const int c1 = min(c0 + kSmallChunk, s1);
-          const int slot = ck % kSlots;
-          if (!waited && ck == (uint32_t)kSlots) {
-            grid_dependency_wait();
-            waited = true;
-            for (uint32_t i = 0; i < npend; ++i)
-              tma_tile3d(smem_u32(smem + i * SM::kSlotBytes + kSmallWBytes), &g.tmap_b, 0, pend_row[i], pend_stage[i],
-                         &full[i]);
-          }
-          mbar_wait(&empty[slot], ((ck / kSlots) + 1) & 1, abort_flag, g.status);
-          // c0 and c1 lie on scale-period boundaries
-          const int64_t off0 = (int64_t)(c0 / PackedFmt<FMT>::kPeriod) * PackedFmt<FMT>::kPeriodBytes;
-          const uint32_t wbytes = (uint32_t)((c1 - c0) / PackedFmt<FMT>::kPeriod * PackedFmt<FMT>::kPeriodBytes);
-          unsigned char* dst = smem + slot * SM::kSlotBytes;
-          mbar_arrive_expect_tx(&full[slot], wbytes + SM::kBBytes);
-          bulk_g2s(dst, tb + off0, wbytes, &full[slot], pol);
-          if (waited) {
-            tma_tile3d(smem_u32(dst + kSmallWBytes), &g.tmap_b, 0, b * g.block_m, c0, &full[slot]);
-          } else {  // ck < kSlots: slot == ck
-            pend_row[npend] = b * g.block_m;
-            pend_stage[npend] = c0;
-            ++npend;
-          }
+    // The whole warp runs the loop; lane 0 issues the weight copies.  GEMM1's
+    // activation rows are gathered from x (fp16, one row per token) four at a
+    // time by the warp's lanes, token = sorted id / top_k; GEMM2's are the
+    // block's rows of a (sorted order), one 3-D box per chunk.  When the
+    // alignment is older than the predecessor (align_early), the first ring's
+    // worth of weight copies go out before the wait on the predecessor and their
+    // activation copies (the predecessor's output) follow it; each slot's
+    // barrier expects both byte counts from the start.
+    const uint64_t pol = policy_evict_first();
+    int32_t* item_rows = reinterpret_cast<int32_t*>(smem + SM::kRows);
+    int32_t* pend_rows = item_rows + 32;  // [kSlots][32]
+    int pend_row[kSlots], pend_stage[kSlots], pend_nst[kSlots];
+    uint32_t npend = 0;
+    bool waited = !g.align_early;
+    uint32_t ck = 0;
+    // activation copies of chunk `stage0` (nst stages) into slot `slot`, rows from `rows`
+    auto issue_act = [&](int slot, int row0, int stage0, int nst, const int32_t* rows) {
+      const uint32_t dst = smem_u32(smem + slot * SM::kSlotBytes + kSmallWBytes);
+      if (kG1) {
+        const uint32_t rows_s = smem_u32(rows);
+        for (int q = lane; q < nst * (BN / 4); q += 32) {
+          const int j = q / (BN / 4), r4 = q % (BN / 4);
+          const uint4 rv = lds128(rows_s + 16 * r4);
+          tma_gather4(dst + j * (BN * 128) + r4 * 512, &g.tmap_b, (stage0 + j) * kStageK,
+                      make_int4((int)rv.x, (int)rv.y, (int)rv.z, (int)rv.w), &full[slot]);
+        }
+      } else if (lane == 0) {
+        tma_tile3d(dst, &g.tmap_b, 0, row0, stage0, &full[slot]);
+      }
+    };
+    for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
+      int b, tile, split, s0, s1;
+      decode_item(plan, w, b, tile, split);
+      stage_range(plan, L, split, s0, s1);
+      const int e = block_expert(g, b);
+      if (e < 0) continue;  // (the consumers skip it too)
+      if (kG1) {
+        __syncwarp();  // the previous item's rows are consumed
+        load_block_rows(g, b, BN, lane, item_rows);
+        __syncwarp();
+      }
+      const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
+      for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
+        const int c1 = min(c0 + kSmallChunk, s1);
+        const int slot = ck % kSlots;
+        if (!waited && ck == (uint32_t)kSlots) {
+          grid_dependency_wait();
+          waited = true;
+          for (uint32_t i = 0; i < npend; ++i) issue_act(i, pend_row[i], pend_stage[i], pend_nst[i], pend_rows + 32 * i);
+        }
+        mbar_wait(&empty[slot], ((ck / kSlots) + 1) & 1, abort_flag, g.status);
+        // c0 and c1 lie on scale-period boundaries
+        const int64_t off0 = (int64_t)(c0 / PackedFmt<FMT>::kPeriod) * PackedFmt<FMT>::kPeriodBytes;
+        const uint32_t wbytes = (uint32_t)((c1 - c0) / PackedFmt<FMT>::kPeriod * PackedFmt<FMT>::kPeriodBytes);
+        const uint32_t bbytes = kG1 ? (uint32_t)((c1 - c0) * BN * 128) : (uint32_t)SM::kBBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[slot], wbytes + bbytes);
+          bulk_g2s(smem + slot * SM::kSlotBytes, tb + off0, wbytes, &full[slot], pol);
+        }
+        __syncwarp();
+        if (waited) {
+          issue_act(slot, b * g.block_m, c0, c1 - c0, item_rows);
+        } else {  // ck < kSlots: slot == ck
+          if (kG1 && lane < BN) pend_rows[32 * npend + lane] = item_rows[lane];
+          pend_row[npend] = b * g.block_m;
+          pend_stage[npend] = c0;
+          pend_nst[npend] = c1 - c0;
+          ++npend;
+          __syncwarp();
         }
       }
-      if (!waited) {
-        grid_dependency_wait();
-        for (uint32_t i = 0; i < npend; ++i)
-          tma_tile3d(smem_u32(smem + i * SM::kSlotBytes + kSmallWBytes), &g.tmap_b, 0, pend_row[i], pend_stage[i],
-                     &full[i]);
-      }
-      // leave no copy in flight
+    }
+    if (!waited) {
+      grid_dependency_wait();
+      for (uint32_t i = 0; i < npend; ++i) issue_act(i, pend_row[i], pend_stage[i], pend_nst[i], pend_rows + 32 * i);
+    }
+    // leave no copy in flight
+    if (lane == 0) {
       for (uint32_t i = 0; i < (uint32_t)kSlots && i < ck; ++i) {
         const uint32_t k = ck - 1 - i;
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&full[k % kSlots], (k / kSlots) & 1) && global_timer_ns() - t0 < 100000000ull) {
-        }
+        mbar_drain(&full[k % kSlots], (k / kSlots) & 1, g.status);
       }
     }
   } else {
@@ -380,12 +411,17 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     const int out_rows = kG1 ? Npad : L.K;                     // rows of the tile that exist
     uint32_t m[kSmallMI][2][4] = {};
     uint32_t ck = 0;
+    float vmax = 0.0f;  // largest |value| stored as fp16 (NaN ignored)
 
     for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
       int b, tile, split, s0, s1;
       decode_item(plan, w, b, tile, split);
       stage_range(plan, L, split, s0, s1);
-      const int e = g.expert_ids[b];
+      const int e = block_expert(g, b);
+      if (e < 0) {  // a block inside n_padded without one of this layer's experts
+        if (cw == 0 && lane == 0 && split == 0) atomicOr(g.status, kStatusRouting);
+        continue;
+      }
       float acc[kSmallMI][NT][4];
 #pragma unroll
       for (int i = 0; i < kSmallMI; ++i)
@@ -491,9 +527,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
             for (int c = 0; c < 2; ++c) {
               const int pos = b * g.block_m + n * 8 + 2 * tq + c;
               const int sid = g.sorted_ids[pos];
+              if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);  // neither a pair nor padding
               const float hg = acc[i][n][c] * gsc + bg;
               const float hu = acc[i][n][2 + c] * gsc + bu;
-              const float a = sid < g.pairs ? act_fn(g.act_kind, hg, hu, g.alpha, g.limit) : 0.0f;
+              const float a = live_sid(sid, g.pairs) ? act_fn(g.act_kind, hg, hu, g.alpha, g.limit) : 0.0f;
+              vmax = fmax_nan(vmax, fabsf(a));
               g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
             }
         } else if (kG1) {  // non-gated: relu(h)^2 of each row, fp16 rows by sorted position
@@ -507,7 +545,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
               for (int c = 0; c < 2; ++c) {
                 const int pos = b * g.block_m + n * 8 + 2 * tq + c;
                 const int sid = g.sorted_ids[pos];
-                const float a = sid < g.pairs ? relu2(acc[i][n][2 * h + c] * gsc + bf) : 0.0f;
+                if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
+                const float hv = acc[i][n][2 * h + c] * gsc + bf;
+                const bool live = live_sid(sid, g.pairs);
+                const float a = live ? relu2(hv) : 0.0f;
+                vmax = fmax_nan(vmax, fmax_nan(a, live ? hv * 0.0f : 0.0f));  // hv * 0: NaN unless finite
                 g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
               }
           }
@@ -523,7 +565,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
               for (int c = 0; c < 2; ++c) {
                 const int pos = b * g.block_m + n * 8 + 2 * tq + c;
                 const int sid = g.sorted_ids[pos];
-                if (sid < g.pairs) g.y_out[(int64_t)sid * L.K + o] = __half_as_ushort(__float2half_rn(acc[i][n][2 * h + c] * gsc + bo));
+                if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
+                if (live_sid(sid, g.pairs)) {
+                  const float y = acc[i][n][2 * h + c] * gsc + bo;
+                  vmax = fmax_nan(vmax, y * 0.0f);  // fp32 y: only a non-finite value is an error
+                  g.y_out[(int64_t)sid * L.K + o] = y;
+                }
               }
           }
         }
@@ -534,6 +581,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     // limit, records the timeout in the status word and the kernel ends
     // normally, so the host reads MOE_ERR_TIMEOUT and the context stays usable.
     if (g.test_starve_wait && blockIdx.x == 0) mbar_wait(starve, 0, abort_flag, g.status);
+    report_epilogue_status(g, vmax, cw == 0 && lane == 0, kStatusBlobFlagsSmall);
   }
   __syncthreads();
 }

@@ -4,8 +4,13 @@
 // PR #28231): deinterleave_moe_mxfp4_w13_for_marlin, _pad_w13 / _pad_w2).
 //
 // Every output byte is written by exactly one thread; reading the source is
-// byte-gather work, so the kernels are simple and run once per layer.
+// byte-gather work, so the kernels are simple and run once per layer.  Before
+// the scales are written, one CTA per expert matrix finds the exponent range of
+// its scales and the power-of-two shift that moves them into the fp16 operand
+// window (common.cuh); the scales are stored shifted and the expert's epilogue
+// factor carries the inverse power.
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -46,6 +51,74 @@ __device__ __forceinline__ int source_row(const RepackArgs& a, int which, int ti
 }
 
 __device__ __forceinline__ uint32_t zero_code(int fmt) { return fmt == MOE_W_INT4_U4B8 ? 8u : 0u; }
+
+// Scale-exponent shift of one expert matrix: blockIdx.x = which * E + e.  The
+// exponent of a finite nonzero INT4 scale is floor(log2 |s|); an MXFP4 scale's is
+// its E8M0 byte (255, NaN, is skipped); NVFP4 needs no shift.  The shift d puts
+// [lo + d, hi + d] inside the window, as close to 0 as possible; when the span is
+// wider than the window it keeps the largest scales exact and flags the blob.
+__global__ void __launch_bounds__(256) repack_shift_kernel(RepackArgs a) {
+  const Layout& L = a.L;
+  const int which = blockIdx.x / L.E, e = blockIdx.x % L.E;
+  int32_t* shift = reinterpret_cast<int32_t*>(a.out + L.shift_off) + which * L.E + e;
+  if (L.fmt == MOE_W_NVFP4) {
+    if (threadIdx.x == 0) *shift = 0;
+    return;
+  }
+  const int red = which ? L.N : L.K;
+  const int64_t rows = which ? L.K : (L.gated ? 2 : 1) * (int64_t)L.N;
+  const int64_t n = rows * (red / L.group);  // scales of one expert
+  const uint8_t* src = which ? a.w2_s : a.w13_s;
+  int lo = INT_MAX, hi = INT_MIN;
+  if (L.fmt == MOE_W_INT4_U4B8) {
+    const uint16_t* sp = reinterpret_cast<const uint16_t*>(src) + (int64_t)e * n;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint32_t bits = sp[i];
+      if ((bits & 0x7F80u) == 0x7F80u || (bits & 0x7FFFu) == 0) continue;  // inf, NaN, zero
+      int ex;
+      frexpf(bf16_bits_to_float((uint16_t)bits), &ex);  // |s| in [2^(ex-1), 2^ex)
+      lo = min(lo, ex - 1);
+      hi = max(hi, ex - 1);
+    }
+  } else {
+    const uint8_t* sp = src + (int64_t)e * n;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+      const int b = sp[i];
+      if (b == 255) continue;
+      lo = min(lo, b);
+      hi = max(hi, b);
+    }
+  }
+  __shared__ int s_lo[8], s_hi[8];
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    s_lo[threadIdx.x >> 5] = lo;
+    s_hi[threadIdx.x >> 5] = hi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) {
+      lo = min(lo, s_lo[w]);
+      hi = max(hi, s_hi[w]);
+    }
+    const bool int4 = L.fmt == MOE_W_INT4_U4B8;
+    const int wmin = int4 ? kInt4ExpMin : kE8m0Min, wmax = int4 ? kInt4ExpMax : kE8m0Max;
+    int d = 0;
+    if (lo <= hi) {
+      const int dlo = wmin - lo, dhi = wmax - hi;
+      if (dlo <= dhi) {
+        d = min(max(0, dlo), dhi);
+      } else {
+        d = dhi;
+        atomicOr(reinterpret_cast<unsigned*>(a.out), int4 ? kFlagInt4Window : kFlagFp4Window);
+      }
+    }
+    *shift = d;
+  }
+}
 
 // One thread per 16-byte unit of packed codes: unit (e, tile, stage, j, r).
 __global__ void repack_codes_kernel(RepackArgs a, int which) {
@@ -107,6 +180,7 @@ __global__ void repack_scales_kernel(RepackArgs a, int which) {
   const uint8_t* src = which ? a.w2_s : a.w13_s;
   const int64_t src_rows = which ? L.K : (L.gated ? 2 : 1) * (int64_t)L.N;
   const int sb = L.fmt == MOE_W_INT4_U4B8 ? 2 : 1;  // source bytes per scale
+  const int32_t* shift = reinterpret_cast<const int32_t*>(a.out + L.shift_off) + which * L.E;
   for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
     const int r = (int)(u % 256);
     const int q = (int)((u / 256) % chunks);
@@ -116,16 +190,25 @@ __global__ void repack_scales_kernel(RepackArgs a, int which) {
     const uint8_t* srow = row >= 0 ? src + ((int64_t)e * src_rows + row) * groups * sb : nullptr;
     uint8_t* dst = a.out + (which ? L.w2_off : L.w13_off) + ((int64_t)e * T + tile) * tile_bytes +
                    stage_offset(L, q * L.period);
+    const int d = shift[e];
     if (L.fmt == MOE_W_INT4_U4B8) {  // group q covers stages 2q, 2q+1
       uint16_t v = 0x3F80;            // 1.0 for padding
-      if (srow && q < groups) v = reinterpret_cast<const uint16_t*>(srow)[q];
+      if (srow && q < groups) {
+        // times 2^d: exact while the result is a normal bf16, which the window guarantees
+        v = reinterpret_cast<const uint16_t*>(srow)[q];
+        if ((v & 0x7F80u) != 0x7F80u && (v & 0x7FFFu) != 0)
+          v = float_to_bf16_bits(ldexpf(bf16_bits_to_float(v), d));
+      }
       reinterpret_cast<uint16_t*>(dst)[r] = v;
     } else if (L.fmt == MOE_W_MXFP4) {  // groups 2q, 2q+1 (32 each)
       uint32_t v = 0;
       for (int g = 0; g < 2; ++g) {
         const int gi = 2 * q + g;
         uint32_t b = 127;  // 2^0 for padding
-        if (srow && gi < groups) b = srow[gi];
+        if (srow && gi < groups) {
+          b = srow[gi];
+          if (b != 255u) b = (uint32_t)min(max((int)b + d, 0), 254);  // 2^d; NaN stays NaN
+        }
         v |= b << (8 * g);
       }
       reinterpret_cast<uint16_t*>(dst)[r] = (uint16_t)v;
@@ -166,8 +249,9 @@ __global__ void repack_misc_kernel(RepackArgs a) {
       reinterpret_cast<uint16_t*>(a.out + L.b2_off)[v2] = c < L.K ? a.b2[(int64_t)e * L.K + c] : (uint16_t)0;
     } else {
       const int e = (int)(u - n13 - n2);
-      float g13 = 1.0f, g2 = 1.0f;
-      if (L.fmt == MOE_W_NVFP4) {
+      const int32_t* shift = reinterpret_cast<const int32_t*>(a.out + L.shift_off);
+      float g13 = ldexpf(1.0f, -shift[e]), g2 = ldexpf(1.0f, -shift[L.E + e]);  // undo the scale shift
+      if (L.fmt == MOE_W_NVFP4) {  // no shift for NVFP4 (every E4M3 scale is exact)
         g13 = a.w13_gs[e];
         g2 = a.w2_gs[e];
       }
@@ -200,8 +284,10 @@ extern "C" int moe_repack_weights(const moe_layer_desc* desc, const void* w13, c
   if ((reinterpret_cast<uintptr_t>(packed) & 255) != 0) return MOE_ERR_INVALID;
   if (desc->fmt == MOE_W_NVFP4 && (!w13_gs || !w2_gs)) return MOE_ERR_INVALID;
   if ((desc->has_bias13 && !b13) || (desc->has_bias2 && !b2)) return MOE_ERR_INVALID;
-  if (desc->w13_interleaved && (2 * desc->inter) % 2 != 0) return MOE_ERR_INVALID;
-  if (desc->w13_interleaved && desc->non_gated) return MOE_ERR_INVALID;
+  // (Interleaved storage needs an even row count and scale / bias rows matching
+  // the weight rows; here every count derives from desc -- 2N rows -- so only
+  // the gating rule can be broken, and make_layout rejects interleaved
+  // non-gated banks.)
   RepackArgs a;
   a.L = L;
   a.interleaved = desc->w13_interleaved != 0;
@@ -219,6 +305,7 @@ extern "C" int moe_repack_weights(const moe_layer_desc* desc, const void* w13, c
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(packed, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;  // header
   const int threads = 256, blocks = 152 * 16;
+  repack_shift_kernel<<<2 * L.E, threads, 0, st>>>(a);  // before the scales and the global factors
   for (int which = 0; which < 2; ++which) {
     repack_codes_kernel<<<blocks, threads, 0, st>>>(a, which);
     repack_scales_kernel<<<blocks, threads, 0, st>>>(a, which);

@@ -5,7 +5,7 @@ in order.  It performs no arithmetic of the layer itself.
 Typical use::
 
     layer = MoELayer.from_numpy(weights, device="cuda")        # repack once
-    out = layer(x, topk_ids, topk_weights)                      # align + forward
+    out = layer(x, topk_ids, topk_weights)                      # aligns inside the forward
 """
 from __future__ import annotations
 
@@ -100,24 +100,38 @@ class MoELayer:
             self._ws = {key: ws}  # keep one workspace alive
         return ws
 
-    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, a: AlignOut,
-                expert_base: int = 0, act: Optional[str] = None, alpha: float = 1.702, limit: float = math.inf,
-                routed_scaling_factor: float = 1.0, post_norm_w: Optional[torch.Tensor] = None,
-                norm_eps: float = 1e-8, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                a: Optional[AlignOut] = None, expert_base: int = 0, act: Optional[str] = None,
+                alpha: float = 1.702, limit: float = math.inf, routed_scaling_factor: float = 1.0,
+                post_norm_w: Optional[torch.Tensor] = None, norm_eps: float = 1e-8,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                block_m: Optional[int] = None, num_routed_ids: Optional[int] = None, stream=None) -> torch.Tensor:
+        """The layer on an alignment from align() (a), or with a = None on the
+        alignment the forward computes itself in its first kernel (block_m chosen
+        by the library unless given)."""
         M, k = topk_ids.shape
         if act is None:  # the layer's own kind: silu_and_mul when gated, relu2 otherwise
             act = "silu_mul" if self.gated else "relu2"
         if out is None:
             out = torch.empty((M, self.K), dtype=torch.bfloat16, device=self.device)
-        ws = workspace if workspace is not None else self.workspace(M, k, a.block_m)
-        B.moe_w4a16_forward(self.desc, self.packed, x, M, k, topk_ids, topk_weights, expert_base, a.sorted_ids,
-                            a.expert_ids, a.n_padded, a.block_m, ACT[act], alpha, limit, routed_scaling_factor,
-                            post_norm_w, norm_eps, out, ws, ws.numel(), stream)
+        if a is not None:
+            bm, s_ids, e_ids, n_pad = a.block_m, a.sorted_ids, a.expert_ids, a.n_padded
+        else:
+            bm = block_m or self.choose_block_m(M, k, num_routed_ids or self.E)
+            s_ids = e_ids = n_pad = None
+        ws = workspace if workspace is not None else self.workspace(M, k, bm)
+        B.moe_w4a16_forward(self.desc, self.packed, x, M, k, topk_ids, topk_weights, expert_base, s_ids, e_ids,
+                            n_pad, bm, ACT[act], alpha, limit, routed_scaling_factor, post_norm_w, norm_eps, out, ws,
+                            ws.numel(), stream)
         return out
 
     def __call__(self, x, topk_ids, topk_weights, expert_base: int = 0, block_m: Optional[int] = None,
-                 num_routed_ids: Optional[int] = None, **kw) -> torch.Tensor:
+                 num_routed_ids: Optional[int] = None, separate_align: bool = False, **kw) -> torch.Tensor:
+        """align + forward.  By default the forward aligns the routing itself (one
+        launch fewer); separate_align = True runs moe_align first, as the pages do."""
+        if not separate_align:
+            return self.forward(x, topk_ids, topk_weights, None, expert_base=expert_base, block_m=block_m,
+                                num_routed_ids=num_routed_ids, **kw)
         a = self.align(topk_ids, expert_base, block_m, num_routed_ids)
         return self.forward(x, topk_ids, topk_weights, a, expert_base=expert_base, **kw)
 
