@@ -48,7 +48,11 @@ class _Layer(ctypes.Structure):
                 ("inter", ctypes.c_int), ("group", ctypes.c_int), ("interleaved", ctypes.c_int),
                 ("w13", ctypes.c_void_p), ("w13_s", ctypes.c_void_p), ("w13_gs", ctypes.c_void_p),
                 ("b13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w2_s", ctypes.c_void_p),
-                ("w2_gs", ctypes.c_void_p), ("b2", ctypes.c_void_p), ("gated", ctypes.c_int)]
+                ("w2_gs", ctypes.c_void_p), ("b2", ctypes.c_void_p), ("gated", ctypes.c_int),
+                ("zero_kind", ctypes.c_int), ("w13_z", ctypes.c_void_p), ("w2_z", ctypes.c_void_p),
+                ("w13_gidx", ctypes.c_void_p), ("w2_gidx", ctypes.c_void_p)]
+
+ZERO_KINDS = {"": 0, "int": 1, "float": 2}
 
 
 class _Batch(ctypes.Structure):
@@ -75,6 +79,8 @@ def lib():
                 getattr(L, n).argtypes = [ctypes.c_uint]
             L.orc_dequant.restype = None
             L.orc_dequant.argtypes = [i32, p, p, i32, i32, i32, p, p]
+            L.orc_dequant_ex.restype = None
+            L.orc_dequant_ex.argtypes = [i32, p, p, p, i32, p, i32, i32, i32, p, p]
             L.orc_align_capacity.restype = i64
             L.orc_align_capacity.argtypes = [i32, i32, i32, i32]
             L.orc_align.restype = i32
@@ -124,15 +130,21 @@ def int4_value(q: int) -> float:
 
 
 def dequant(fmt: str, codes: np.ndarray, scales: np.ndarray, group: int,
-            row_map: Optional[np.ndarray] = None) -> np.ndarray:
-    """One expert's matrix: codes uint8 [R, C/2], scales [R, C/g] -> float32 [rows, C]."""
+            row_map: Optional[np.ndarray] = None, zeros: Optional[np.ndarray] = None, zero_kind: str = "",
+            gidx: Optional[np.ndarray] = None) -> np.ndarray:
+    """One expert's matrix: codes uint8 [R, C/2], scales [R, C/g] (and INT4 zero
+    points [R, C/g], uint8 or bf16 bits, and act-order groups gidx int32 [C])
+    -> float32 [rows, C].  group <= 0: one group per row."""
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales)
     rows = codes.shape[0] if row_map is None else len(row_map)
     cols = codes.shape[1] * 2
     out = np.empty((rows, cols), dtype=np.float32)
     rm = None if row_map is None else np.ascontiguousarray(row_map, dtype=np.int32)
-    lib().orc_dequant(FMT_CODES[fmt], _ptr(codes), _ptr(scales), rows, cols, group, _ptr(rm), _ptr(out))
+    z = None if zeros is None else np.ascontiguousarray(zeros)
+    gi = None if gidx is None else np.ascontiguousarray(gidx, dtype=np.int32)
+    lib().orc_dequant_ex(FMT_CODES[fmt], _ptr(codes), _ptr(scales), _ptr(z), ZERO_KINDS[zero_kind], _ptr(gi),
+                         rows, cols, group, _ptr(rm), _ptr(out))
     return out
 
 
@@ -169,10 +181,13 @@ def _structs(W, X, expert_base, act, alpha, limit, rsf, norm_eps, post_norm, kee
         keep.append(a)
         return _ptr(a)
 
+    zk = getattr(W, "zero_kind", "")
     layer = _Layer(FMT_CODES[W.fmt], W.E, W.K, W.N, W.group, int(W.interleaved),
                    c(W.w13, np.uint8), c(W.w13_s), c(W.w13_gs, np.float32), c(W.b13, np.uint16),
                    c(W.w2, np.uint8), c(W.w2_s), c(W.w2_gs, np.float32), c(W.b2, np.uint16),
-                   int(getattr(W, "gated", True)))
+                   int(getattr(W, "gated", True)), ZERO_KINDS[zk], c(getattr(W, "w13_z", None)),
+                   c(getattr(W, "w2_z", None)), c(getattr(W, "w13_gidx", None), np.int32),
+                   c(getattr(W, "w2_gidx", None), np.int32))
     pnw = X.post_norm_w if post_norm else None
     b = _Batch(M, k, expert_base, ACT_CODES[act], alpha, limit, rsf, norm_eps,
                c(X.x, np.uint16), c(X.topk_ids, np.int32), c(X.topk_weights, np.float32),

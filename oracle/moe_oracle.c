@@ -13,7 +13,10 @@
  *               test_fused_marlin_moe_large_non_ep_schedule: quant_type uint4b8;
  *               E2M1 / E8M0 / E4M3 from the OCP microscaling and FP8 formats, which
  *               the pages name but do not define);
- *   dequant     W = (q-8)*s (int4, group along the reduction dim),
+ *   dequant     W = (q-8)*s (int4, group along the reduction dim), or with the INT4
+ *               variants W = (q - z)*s, z an integer or bf16 zero point per group,
+ *               groups of 32 / 64 / 128 / a whole row, or given per reduction index
+ *               by g_idx (act-order),
  *               W = e2m1*2^(b-127) (MXFP4, one E8M0 byte per 32),
  *               W = e2m1*e4m3*gs[e] (NVFP4, one E4M3 per 16, one fp32 global
  *               scale per expert shared by gate and up: "013-moe-middle-tiles.py",
@@ -147,27 +150,53 @@ static double scale_value(int fmt, const void* scales, long idx) {
     return orc_e4m3_value(((const uint8_t*)scales)[idx]);
 }
 
-static int scale_bytes(int fmt) { return fmt == ORC_INT4 ? 2 : 1; }
 
 /*
  * Dequantise logical rows [0, rows) of one expert's matrix, cols along the
  * reduction dimension, into out[rows][cols] (without the NVFP4 global scale,
  * which the caller applies to the fp64 sum).  row_map[r] gives the stored row
  * of logical row r (identity when NULL); it is how interleaved gate/up rows are
- * read.  Every product q*s is exact in binary32 for the three formats.
+ * read.
+ *
+ * INT4 variants (the w*_zeros, is_zp_float, g_idx and group_blocks of
+ * fused_marlin_moe / the Marlin template in "Marlin MoE kernel occupancy ..."
+ * (sglang PR #31552)): element c of a row belongs to group gidx[c] when gidx
+ * is given (act-order), else to c / group; group <= 0 means one group per row
+ * (channelwise).  With zero_kind 0 the code is uint4b8, W = (q - 8) * s; with
+ * zero_kind 1 the group's zero point is an integer byte z, W = (q - z) * s;
+ * with zero_kind 2 a bf16 value z, W = (q - z) * s.  zeros hold one entry per
+ * (row, group), like the scales.  Every product is exact in binary32 except
+ * float zeros, whose (q - z) * s is rounded once to binary32.
  */
-void orc_dequant(int fmt, const uint8_t* codes, const void* scales, int rows, int cols, int group,
-                 const int32_t* row_map, float* out) {
-    long bpr = cols / 2, spr = cols / group;
+void orc_dequant_ex(int fmt, const uint8_t* codes, const void* scales, const void* zeros, int zero_kind,
+                    const int32_t* gidx, int rows, int cols, int group, const int32_t* row_map, float* out) {
+    long bpr = cols / 2;
+    if (group <= 0) group = cols;
+    long spr = cols / group;
 #pragma omp parallel for schedule(static)
     for (int r = 0; r < rows; ++r) {
         long sr = row_map ? row_map[r] : r;
         const uint8_t* crow = codes + sr * bpr;
         for (long c = 0; c < cols; ++c) {
-            double v = code_value(fmt, nibble(crow, c)) * scale_value(fmt, scales, sr * spr + c / group);
+            long g = gidx ? (long)gidx[c] : c / group;
+            double sv = scale_value(fmt, scales, sr * spr + g);
+            unsigned q = nibble(crow, c);
+            double v;
+            if (fmt != ORC_INT4 || zero_kind == 0) {
+                v = code_value(fmt, q) * sv;
+            } else if (zero_kind == 1) {
+                v = ((double)q - (double)((const uint8_t*)zeros)[sr * spr + g]) * sv;
+            } else {
+                v = ((double)q - orc_bf16_value(((const uint16_t*)zeros)[sr * spr + g])) * sv;
+            }
             out[(long)r * cols + c] = (float)v;
         }
     }
+}
+
+void orc_dequant(int fmt, const uint8_t* codes, const void* scales, int rows, int cols, int group,
+                 const int32_t* row_map, float* out) {
+    orc_dequant_ex(fmt, codes, scales, NULL, 0, NULL, rows, cols, group, row_map, out);
 }
 
 /* ------------------------------------------------------------------ align */
@@ -238,7 +267,29 @@ typedef struct {
     const float* w2_gs;   /* [E] or NULL */
     const uint16_t* b2;   /* [E, K] bf16 or NULL */
     int gated;            /* 1: gate and up rows, act on (gate, up); 0: N rows, relu^2 */
+    int zero_kind;        /* INT4 zero points: 0 none (uint4b8), 1 integer bytes, 2 bf16 values */
+    const void* w13_z;    /* [E, R, K/g] zero points, or NULL */
+    const void* w2_z;     /* [E, K, N/g] */
+    const int32_t* w13_gidx;  /* [E, K] group of each reduction index (act-order), or NULL */
+    const int32_t* w2_gidx;   /* [E, N] */
 } orc_layer;
+
+/* Groups per row of a matrix with `cols` reduction elements (group <= 0: one). */
+static long n_groups(int group, int cols) { return group <= 0 ? 1 : cols / group; }
+
+/* Dequantised w13 (logical rows, gate block then up block) and w2 of expert e. */
+static void dequant_expert(const orc_layer* L, int e, const int32_t* rmap, float* W13, float* W2) {
+    const int K = L->hidden, N = L->inter, R = L->gated ? 2 * N : N;
+    const long sb = L->fmt == ORC_INT4 ? 2 : 1;                 /* scale bytes */
+    const long zb = L->zero_kind == 2 ? 2 : 1;                  /* zero bytes */
+    const long g13 = n_groups(L->group, K), g2 = n_groups(L->group, N);
+    orc_dequant_ex(L->fmt, L->w13 + (long)e * R * (K / 2), (const uint8_t*)L->w13_s + (long)e * R * g13 * sb,
+                   L->w13_z ? (const uint8_t*)L->w13_z + (long)e * R * g13 * zb : NULL, L->zero_kind,
+                   L->w13_gidx ? L->w13_gidx + (long)e * K : NULL, R, K, L->group, rmap, W13);
+    orc_dequant_ex(L->fmt, L->w2 + (long)e * K * (N / 2), (const uint8_t*)L->w2_s + (long)e * K * g2 * sb,
+                   L->w2_z ? (const uint8_t*)L->w2_z + (long)e * K * g2 * zb : NULL, L->zero_kind,
+                   L->w2_gidx ? L->w2_gidx + (long)e * N : NULL, K, N, L->group, NULL, W2);
+}
 
 typedef struct {
     int M, top_k, expert_base, act;
@@ -299,10 +350,12 @@ int orc_forward(const orc_layer* L, const orc_batch* X, const int32_t* tokens, i
                 uint16_t* out_bf16, double* out_acc) {
     const int K = L->hidden, N = L->inter, E = L->num_experts, k = X->top_k;
     const int R = L->gated ? 2 * N : N;  /* rows of w13 */
-    if (K <= 0 || N <= 0 || E <= 0 || k <= 0 || L->group <= 0) return -1;
+    if (K <= 0 || N <= 0 || E <= 0 || k <= 0 || L->group == 0) return -1;
     if (!L->gated && X->act != ORC_RELU2) return -1;
     if (L->gated && X->act == ORC_RELU2) return -1;
-    if (K % L->group || N % L->group || K % 2 || N % 2) return -1;
+    if ((L->group > 0 && (K % L->group || N % L->group)) || K % 2 || N % 2) return -1;
+    if (L->fmt != ORC_INT4 && (L->zero_kind || L->w13_gidx || L->w2_gidx || L->group < 0)) return -1;
+    if (L->zero_kind && (!L->w13_z || !L->w2_z)) return -1;
     double* acc_out = (double*)calloc((size_t)n_tokens * K, sizeof(double));
     double* nsq = (double*)calloc((size_t)n_tokens * k, sizeof(double));
     float* W13 = (float*)malloc(sizeof(float) * (size_t)R * K);
@@ -323,18 +376,13 @@ int orc_forward(const orc_layer* L, const orc_batch* X, const int32_t* tokens, i
             float s = (float)(1.0 + orc_bf16_value(X->post_norm_w[c]));  /* fp32 add, as torch */
             nw[c] = round_bf16((double)s);
         }
-    const long sb = scale_bytes(L->fmt);
     for (int e = 0; e < E; ++e) {
         int touched = 0;
         for (int i = 0; i < n_tokens && !touched; ++i)
             for (int j = 0; j < k; ++j)
                 if (X->topk_ids[(long)tokens[i] * k + j] - X->expert_base == e) { touched = 1; break; }
         if (!touched) continue;
-        orc_dequant(L->fmt, L->w13 + (long)e * R * (K / 2),
-                    (const uint8_t*)L->w13_s + (long)e * R * (K / L->group) * sb, R, K, L->group,
-                    rmap, W13);
-        orc_dequant(L->fmt, L->w2 + (long)e * K * (N / 2),
-                    (const uint8_t*)L->w2_s + (long)e * K * (N / L->group) * sb, K, N, L->group, NULL, W2);
+        dequant_expert(L, e, rmap, W13, W2);
         for (int i = 0; i < n_tokens; ++i) {
             int t = tokens[i];
             for (int j = 0; j < k; ++j) {
@@ -380,11 +428,7 @@ int orc_ffn_pair(const orc_layer* L, const orc_batch* X, int e, int t, double* h
     int32_t* rmap = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
     if (!W13 || !W2 || !rmap) { free(W13); free(W2); free(rmap); return -1; }
     for (int r = 0; r < R; ++r) rmap[r] = (L->gated && L->interleaved) ? 2 * (r % N) + (r / N) : r;
-    const long sb = scale_bytes(L->fmt);
-    orc_dequant(L->fmt, L->w13 + (long)e * R * (K / 2),
-                (const uint8_t*)L->w13_s + (long)e * R * (K / L->group) * sb, R, K, L->group, rmap, W13);
-    orc_dequant(L->fmt, L->w2 + (long)e * K * (N / 2),
-                (const uint8_t*)L->w2_s + (long)e * K * (N / L->group) * sb, K, N, L->group, NULL, W2);
+    dequant_expert(L, e, rmap, W13, W2);
     ffn_pair(L, X, e, t, W13, W2, h, a, y);
     free(W13); free(W2); free(rmap);
     return 0;

@@ -73,10 +73,13 @@ class Workload:
     zipf_s: float = 1.2
     gated: bool = True             # False: w1 has N rows and act is relu2
     x_scale: float = 1.0           # x ~ N(0, x_scale^2)
+    group_size: int = 0            # INT4: 0 = the format's 128; 32 / 64 / 128; -1 = one group per row
+    zero_kind: str = ""            # INT4 zero points: "" (uint4b8), "int" (bytes 0..15), "float" (bf16)
+    act_order: bool = False        # INT4: groups given per reduction index (g_idx) in a random order
 
     @property
     def group(self) -> int:
-        return GROUP[self.fmt]
+        return self.group_size or GROUP[self.fmt]
 
     @property
     def n_ids(self) -> int:
@@ -161,6 +164,13 @@ class LayerWeights:
     w2_gs: Optional[np.ndarray]
     b2: Optional[np.ndarray]
     gated: bool = True
+    zero_kind: str = ""                 # INT4 zero points: "", "int" or "float"
+    w13_z: Optional[np.ndarray] = None  # [E, R, K/g] uint8 (int) or uint16 bf16 bits (float)
+    w2_z: Optional[np.ndarray] = None   # [E, K, N/g]
+    w13_gidx: Optional[np.ndarray] = None  # int32 [E, K]: group of each reduction index (act-order)
+    w2_gidx: Optional[np.ndarray] = None   # int32 [E, N]
+    w13_perm: Optional[np.ndarray] = None  # int32 [E, K]: reduction indices ordered by group (sort_indices)
+    w2_perm: Optional[np.ndarray] = None   # int32 [E, N]
 
 
 def _scales(rng: np.random.Generator, fmt: str, shape) -> np.ndarray:
@@ -174,15 +184,33 @@ def _scales(rng: np.random.Generator, fmt: str, shape) -> np.ndarray:
     raise ValueError(fmt)
 
 
+def _groups(g: int, cols: int) -> int:
+    return 1 if g < 0 else cols // g
+
+
+def _act_order(rng: np.random.Generator, E: int, cols: int, g: int):
+    """Per expert a random order of the reduction indices; index k belongs to
+    group (its place in that order) // g, as GPTQ's act-order assigns them.  Returns
+    g_idx [E, cols] and sort_indices [E, cols] (indices by ascending group, ties in
+    index order)."""
+    size = cols if g < 0 else g
+    gidx = np.empty((E, cols), dtype=np.int32)
+    for e in range(E):
+        order = rng.permutation(cols)
+        gidx[e, order] = np.arange(cols) // size
+    perm = np.argsort(gidx, axis=1, kind="stable").astype(np.int32)
+    return gidx, perm
+
+
 def make_weights(wl: Workload, seed: int) -> LayerWeights:
     rng = np.random.Generator(np.random.PCG64(seed))
     E, K, N, g = wl.E, wl.K, wl.N, wl.group
     R = 2 * N if wl.gated else N  # rows of w13
     # every code value equally likely: uniform bytes give uniform nibbles
     w13 = rng.integers(0, 256, size=(E, R, K // 2), dtype=np.uint8)
-    w13_s = _scales(rng, wl.fmt, (E, R, K // g))
+    w13_s = _scales(rng, wl.fmt, (E, R, _groups(g, K)))
     w2 = rng.integers(0, 256, size=(E, K, N // 2), dtype=np.uint8)
-    w2_s = _scales(rng, wl.fmt, (E, K, N // g))
+    w2_s = _scales(rng, wl.fmt, (E, K, _groups(g, N)))
     w13_gs = w2_gs = None
     if wl.fmt == FMT_NVFP4:
         w13_gs = rng.uniform(0.008, 0.012, size=E).astype(np.float32)
@@ -191,8 +219,18 @@ def make_weights(wl: Workload, seed: int) -> LayerWeights:
     if wl.bias_std > 0:
         b13 = to_bf16_bits(rng.normal(0.0, wl.bias_std, size=(E, R)).astype(np.float32))
         b2 = to_bf16_bits(rng.normal(0.0, wl.bias_std, size=(E, K)).astype(np.float32))
+    extra = {}
+    if wl.zero_kind == "int":  # a zero point per (row, group), uniform over the 16 codes
+        extra["w13_z"] = rng.integers(0, 16, size=w13_s.shape, dtype=np.uint8)
+        extra["w2_z"] = rng.integers(0, 16, size=w2_s.shape, dtype=np.uint8)
+    elif wl.zero_kind == "float":  # HQQ-style float zero points in the code range
+        extra["w13_z"] = to_bf16_bits(rng.uniform(0.0, 15.0, size=w13_s.shape).astype(np.float32))
+        extra["w2_z"] = to_bf16_bits(rng.uniform(0.0, 15.0, size=w2_s.shape).astype(np.float32))
+    if wl.act_order:
+        extra["w13_gidx"], extra["w13_perm"] = _act_order(rng, E, K, g)
+        extra["w2_gidx"], extra["w2_perm"] = _act_order(rng, E, N, g)
     return LayerWeights(wl.fmt, E, K, N, g, wl.interleaved, w13, w13_s, w13_gs, b13,
-                        w2, w2_s, w2_gs, b2, gated=wl.gated)
+                        w2, w2_s, w2_gs, b2, gated=wl.gated, zero_kind=wl.zero_kind, **extra)
 
 
 # ---------------------------------------------------------------- per-batch inputs
