@@ -57,8 +57,13 @@ typedef enum moe_status {
 
 /* Weight formats.  Codes are 4 bits, two per byte, element 2j in the low nibble
  * and element 2j+1 in the high nibble of byte j of a row.
- *   INT4_U4B8: code q stands for q - 8 ("uint4b8"); one bf16 scale per group of
- *              group_size (128) along the reduction dimension.
+ *   INT4_U4B8: code q stands for q - 8 ("uint4b8"), or q - z with a zero point z
+ *              (moe_layer_desc.zero_kind); one bf16 scale per group of
+ *              group_size (32, 64, 128, or -1: one group per row) along the
+ *              reduction dimension, groups given per reduction index by g_idx
+ *              when act_order (the w*_zeros / is_zp_float / g_idx /
+ *              sort_indices / group_blocks of fused_marlin_moe and the Marlin
+ *              template, "Marlin MoE kernel occupancy ..." (sglang PR #31552)).
  *   MXFP4:     E2M1 codes; one E8M0 scale byte (2^(b-127)) per 32.
  *   NVFP4:     E2M1 codes; one FP8 E4M3 scale per 16, times one fp32 global
  *              scale per expert (the same for gate and up rows). */
@@ -81,12 +86,17 @@ typedef struct moe_layer_desc {
     int32_t hidden;           /* K: model width (GEMM1 reduction, GEMM2 output); % 64 == 0, and
                                  % 128 == 0 for INT4 */
     int32_t inter;            /* N: expert intermediate width; % group_size == 0 */
-    int32_t group_size;       /* 128 (INT4), 32 (MXFP4) or 16 (NVFP4) */
+    int32_t group_size;       /* INT4: 32, 64, 128 or -1 (one group per row); MXFP4 32; NVFP4 16 */
     int32_t w13_interleaved;  /* 1: w13 rows stored gate0, up0, gate1, up1, ... (GPT-OSS) */
     int32_t has_bias13;       /* 1: per-expert bf16 bias on GEMM1 outputs */
     int32_t has_bias2;        /* 1: per-expert bf16 bias on GEMM2 outputs */
     int32_t non_gated;        /* 0: w13 holds gate and up rows (2N); 1: w13 holds N rows and
                                  the activation is MOE_ACT_RELU2 (w13_interleaved must be 0) */
+    int32_t zero_kind;        /* INT4 only: 0 none (uint4b8); 1 integer zero points, one byte
+                                 0..15 per (row, group); 2 float zero points (is_zp_float),
+                                 one bf16 per (row, group); W = (q - z) * s */
+    int32_t act_order;        /* INT4 only: 1 = both matrices carry g_idx / sort_indices
+                                 (groups of group_size indices each; group_size 32..128) */
 } moe_layer_desc;
 
 /* ------------------------------------------------------------------ repack
@@ -118,6 +128,41 @@ int64_t moe_repack_size(const moe_layer_desc* desc);
 int moe_repack_weights(const moe_layer_desc* desc, const void* w13, const void* w13_s,
                        const float* w13_gs, const void* b13, const void* w2, const void* w2_s,
                        const float* w2_gs, const void* b2, void* packed, void* stream);
+
+/* The checkpoint tensors of one bank, for moe_repack_weights_ex (device
+ * pointers; those a bank does not have are NULL). */
+typedef struct moe_repack_tensors {
+    const void* w13;              /* uint8 [E, R, K/2] */
+    const void* w13_s;            /* [E, R, K/g] */
+    const float* w13_gs;          /* fp32 [E] (NVFP4) */
+    const void* b13;              /* bf16 [E, R] */
+    const void* w13_zeros;        /* [E, R, K/g]: uint8 (zero_kind 1) or bf16 (zero_kind 2) */
+    const int32_t* w13_g_idx;     /* int32 [E, K]: group of each reduction index (act_order) */
+    const int32_t* w13_sort_indices; /* int32 [E, K]: reduction indices by ascending group */
+    const void* w2;               /* uint8 [E, K, N/2] */
+    const void* w2_s;             /* [E, K, N/g] */
+    const float* w2_gs;           /* fp32 [E] (NVFP4) */
+    const void* b2;               /* bf16 [E, K] */
+    const void* w2_zeros;         /* [E, K, N/g] */
+    const int32_t* w2_g_idx;      /* int32 [E, N] */
+    const int32_t* w2_sort_indices;  /* int32 [E, N] */
+} moe_repack_tensors;
+
+/* moe_repack_weights with the INT4 variants: zero points (desc->zero_kind),
+ * act-order (desc->act_order) and group sizes 32 / 64 / 128 / -1.  With
+ * act_order the reduction dimension of each expert matrix is stored in
+ * sort_indices order, so that its groups are contiguous; w2's order is folded
+ * into the order of w13's output features (and their bias), so GEMM1 writes
+ * the activations in the order GEMM2 reads them, and the forward permutes x's
+ * columns per expert as it places the routed rows.  The groups must hold
+ * group_size indices each (g_idx[sort_indices[k]] == k / group_size); a bank
+ * that breaks this marks the blob, and forwards on it report
+ * MOE_ERR_UNSUPPORTED.  Arithmetic: with integer zero points (q - z) * s may
+ * need 12 significant bits and is rounded once to fp16 (relative error <=
+ * 2^-12); with float zero points q * s - z * s is formed in fp16 (z * s rounded
+ * at repack, one more rounding in the product).  Returns MOE_ERR_INVALID for a
+ * missing tensor the descriptor requires. */
+int moe_repack_weights_ex(const moe_layer_desc* desc, const moe_repack_tensors* t, void* packed, void* stream);
 
 /* ------------------------------------------------------------------ align
  * Routing alignment ("013-moe-middle-tiles.py", kernel_fn: moe_align_block_size;

@@ -46,7 +46,16 @@ def test_repack_size_rules(lib):
     assert lib.moe_repack_size(D(0, 8, 512, 1024, 128, 0, 1, 1)) > 0
     assert lib.moe_repack_size(D(1, 32, 2880, 2880, 32, 1, 1, 1)) > 0     # tile padding allowed
     assert lib.moe_repack_size(D(2, 32, 4096, 4096, 16, 0, 0, 0)) > 0
-    for bad in [D(0, 8, 512, 1024, 64, 0, 0, 0),      # wrong group for int4
+    for g in (32, 64, 128, -1):                       # INT4 group sizes
+        assert lib.moe_repack_size(D(0, 8, 512, 1024, g, 0, 1, 1)) > 0
+    assert lib.moe_repack_size(D(0, 8, 512, 1024, 64, 0, 1, 1, 0, 1, 1)) > 0  # zero points + act-order
+    assert lib.moe_repack_size(D(0, 8, 512, 1024, 32, 0, 1, 1, 0, 2, 0)) > 0  # float zero points
+    for bad in [D(0, 8, 512, 1024, 96, 0, 0, 0),      # not a group size for int4
+                D(0, 8, 512, 1024, 16, 0, 0, 0),
+                D(0, 8, 512, 1024, -1, 0, 0, 0, 0, 0, 1),  # act-order needs group sizes
+                D(0, 8, 512, 1024, 128, 0, 0, 0, 0, 3, 0),  # unknown zero kind
+                D(1, 8, 512, 512, 32, 0, 0, 0, 0, 1, 0),    # zero points are INT4-only
+                D(2, 8, 512, 512, 16, 0, 0, 0, 0, 0, 1),    # act-order is INT4-only
                 D(0, 8, 576, 1024, 128, 0, 0, 0),     # int4 hidden % 128
                 D(1, 8, 2880, 2890, 32, 0, 0, 0),     # inter % group
                 D(1, 8, 2900, 2880, 32, 0, 0, 0),     # hidden % 64

@@ -19,7 +19,7 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE
 MOE_W_INT4_U4B8, MOE_W_MXFP4, MOE_W_NVFP4 = 0, 1, 2
 MOE_ACT_SILU_MUL, MOE_ACT_SIGMOID_ALPHA, MOE_ACT_RELU2 = 0, 1, 2
 
-EXPORTED = ("moe_repack_size", "moe_repack_weights", "moe_align_capacity", "moe_align", "moe_choose_block_m",
+EXPORTED = ("moe_repack_size", "moe_repack_weights", "moe_repack_weights_ex", "moe_align_capacity", "moe_align", "moe_choose_block_m",
             "moe_workspace_size", "moe_w4a16_forward", "moe_w4a16_forward_noalloc", "moe_get_status",
             "moe_set_trace_events", "moe_set_test_starve_wait", "moe_status_string", "moe_requant_fp8",
             "moe_requant_launch_geometry")
@@ -35,7 +35,14 @@ class MoeError(RuntimeError):
 class moe_layer_desc(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("inter", ctypes.c_int32), ("group_size", ctypes.c_int32), ("w13_interleaved", ctypes.c_int32),
-                ("has_bias13", ctypes.c_int32), ("has_bias2", ctypes.c_int32), ("non_gated", ctypes.c_int32)]
+                ("has_bias13", ctypes.c_int32), ("has_bias2", ctypes.c_int32), ("non_gated", ctypes.c_int32),
+                ("zero_kind", ctypes.c_int32), ("act_order", ctypes.c_int32)]
+
+
+class moe_repack_tensors(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "w13", "w13_s", "w13_gs", "b13", "w13_zeros", "w13_g_idx", "w13_sort_indices",
+        "w2", "w2_s", "w2_gs", "b2", "w2_zeros", "w2_g_idx", "w2_sort_indices")]
 
 
 _lib = None
@@ -58,6 +65,7 @@ def load(path: str = ""):
             sig = {
                 "moe_repack_size": (i64, [D]),
                 "moe_repack_weights": (i32, [D, p, p, p, p, p, p, p, p, p, p]),
+                "moe_repack_weights_ex": (i32, [D, ctypes.POINTER(moe_repack_tensors), p, p]),
                 "moe_align_capacity": (i64, [i32, i32, i32, i32]),
                 "moe_align": (i32, [p, i32, i32, i32, i32, i32, p, p, p, p]),
                 "moe_choose_block_m": (i32, [D, i32, i32, i32]),
@@ -120,6 +128,13 @@ def moe_repack_weights(desc, w13, w13_s, w13_gs, b13, w2, w2_s, w2_gs, b2, packe
     return _check("moe_repack_weights", load().moe_repack_weights(
         ctypes.byref(desc), _p(w13), _p(w13_s), _p(w13_gs), _p(b13), _p(w2), _p(w2_s), _p(w2_gs), _p(b2),
         _p(packed), _stream(stream)))
+
+
+def moe_repack_weights_ex(desc, tensors: dict, packed, stream=None):
+    """tensors: the moe_repack_tensors fields by name (tensors or None)."""
+    t = moe_repack_tensors(**{k: _p(v) for k, v in tensors.items()})
+    return _check("moe_repack_weights_ex", load().moe_repack_weights_ex(
+        ctypes.byref(desc), ctypes.byref(t), _p(packed), _stream(stream)))
 
 
 def moe_align_capacity(M: int, top_k: int, num_experts: int, block_m: int) -> int:

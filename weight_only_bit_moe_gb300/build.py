@@ -13,7 +13,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build", platform.machine())
 LIB = os.path.join(HERE, "_build", f"libmoe_w4a16_{platform.machine()}.so")
-SOURCES = ["align.cu", "repack.cu", "gemm_int4.cu", "gemm_mxfp4.cu", "gemm_nvfp4.cu", "combine.cu", "requant.cu",
+SOURCES = ["align.cu", "repack.cu", "gemm_int4.cu", "gemm_int4x.cu", "gemm_mxfp4.cu", "gemm_nvfp4.cu", "combine.cu",
+           "requant.cu",
            "api.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

@@ -61,23 +61,31 @@ __device__ __forceinline__ int local_expert(const int32_t* ids, int p, int base,
   return (e >= 0 && e < E) ? e : -1;
 }
 
-// One routed row into sorted order: xs[pos] = fp16(x[token]), by the calling
-// warp (16-byte chunks, four in flight per lane).
-__device__ __forceinline__ void copy_row_f16(const PrologueArgs& a, int token, int64_t pos, int lane) {
-  const uint4* src = reinterpret_cast<const uint4*>(a.x + (int64_t)token * a.K);
+// Columns [8c, 8c+8) of token row `token` of x as fp16 (exact inside the fp16
+// range, beyond it infinity), in expert e's column order for act-order banks.
+__device__ __forceinline__ uint4 x_chunk_f16(const PrologueArgs& a, int token, int e, int c) {
+  const uint16_t* row = a.x + (int64_t)token * a.K;
+  uint4 v;
+  if (!a.perm13) {
+    v = __ldg(reinterpret_cast<const uint4*>(row) + c);
+  } else {
+    const int4* pp = reinterpret_cast<const int4*>(a.perm13 + (int64_t)e * a.K + 8 * c);
+    const int4 p0 = __ldg(pp), p1 = __ldg(pp + 1);
+    const int idx[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = (uint32_t)__ldg(row + idx[2 * i]) | ((uint32_t)__ldg(row + idx[2 * i + 1]) << 16);
+    v = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+}
+
+// One routed row into sorted order: xs[pos] = fp16(x[token]) (columns in expert
+// e's order for act-order banks), by the calling warp (16-byte chunks).
+__device__ __forceinline__ void copy_row_f16(const PrologueArgs& a, int token, int e, int64_t pos, int lane) {
   uint4* dst = reinterpret_cast<uint4*>(a.xs + pos * a.K);
   const int chunks = a.K / 8;
-  for (int c0 = 0; c0 < chunks; c0 += 128) {
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (c0 + 32 * i + lane < chunks) v[i] = __ldg(src + c0 + 32 * i + lane);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (c0 + 32 * i + lane < chunks)
-        dst[c0 + 32 * i + lane] = make_uint4(bf16x2_to_f16x2(v[i].x), bf16x2_to_f16x2(v[i].y),
-                                             bf16x2_to_f16x2(v[i].z), bf16x2_to_f16x2(v[i].w));
-  }
+  for (int c = lane; c < chunks; c += 32) dst[c] = x_chunk_f16(a, token, e, c);
 }
 
 // The one-warp alignment of align_few: writes the pairs, the run experts and
@@ -117,7 +125,8 @@ __device__ void align_few(const PrologueArgs& a) {
   __syncthreads();
   // routed rows into sorted order: warp w copies pair w's
   const int w = tid >> 5;
-  if (a.xs && w < a.pairs && few_pos[w] >= 0) copy_row_f16(a, w / a.top_k, few_pos[w], lane);
+  if (a.xs && w < a.pairs && few_pos[w] >= 0)
+    copy_row_f16(a, w / a.top_k, local_expert(a.topk_ids, w, a.expert_base, a.E), few_pos[w], lane);
 }
 
 // The counting sort of the first G CTAs (c = this CTA), described above.
@@ -247,15 +256,13 @@ __device__ void align_many(const PrologueArgs& a, int G, int c, unsigned char* s
   //    16-byte chunks of the chunk's rows (the positions are this CTA's own writes)
   __syncthreads();
   const int chunks = a.K / 8;
-  const uint4* src = reinterpret_cast<const uint4*>(a.x);
   uint4* dst = reinterpret_cast<uint4*>(a.xs);
   for (int64_t i = tid; i < (int64_t)(q1 - q0) * chunks; i += kAlignThreads) {
     const int p = q0 + (int)(i / chunks), cc = (int)(i % chunks);
     const int pos = a.pair_pos[p];
     if (pos < 0) continue;
-    const uint4 v = __ldg(src + (int64_t)(p / a.top_k) * chunks + cc);
-    dst[(int64_t)pos * chunks + cc] =
-        make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+    const int e = a.perm13 ? local_expert(topk_ids, p, expert_base, E) : 0;
+    dst[(int64_t)pos * chunks + cc] = x_chunk_f16(a, p / a.top_k, e, cc);
   }
 }
 
@@ -311,8 +318,12 @@ __global__ void __launch_bounds__(kAlignThreads, 1) prologue_kernel(const __grid
       const int c = (int)(i - pos * chunks);
       const int sid = a.given_sorted[pos];
       if ((unsigned)sid >= (unsigned)a.pairs) continue;  // padding (or an id no pair has)
-      const uint4 v = src[(int64_t)(sid / a.top_k) * chunks + c];
-      dst[i] = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+      int e = 0;
+      if (a.perm13) {
+        e = a.given_expert_ids[pos / a.block_m];
+        if ((unsigned)e >= (unsigned)a.E) continue;  // (the GEMMs skip and report the block)
+      }
+      dst[i] = x_chunk_f16(a, sid / a.top_k, e, c);
     }
   }
 }

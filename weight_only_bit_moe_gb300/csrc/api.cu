@@ -73,9 +73,10 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   w->align_off = off;
   off = round_up64(off + (cap + w->blocks + 1 + pairs) * 4, 256);
   // x as fp16: its own rows [M, K] for the register-fed kernels (block_m <= 32),
-  // the routed rows in sorted order [cap, K] for the tcgen05 kernels
+  // the routed rows in sorted order [cap, K] for the tcgen05 kernels and for
+  // act-order banks (whose x columns follow each expert's order)
   w->xh_off = off;
-  off = round_up64(off + (block_m <= 32 ? (int64_t)M : cap) * L.K * 2, 256);
+  off = round_up64(off + (block_m <= 32 && !L.act_order ? (int64_t)M : cap) * L.K * 2, 256);
   w->a_off = off;
   off = round_up64(off + cap * L.Npad * 2, 256);
   w->y_off = off;
@@ -94,6 +95,7 @@ cudaError_t launch_gemm(int fmt, bool small, int stage, int bn, const GemmArgs& 
     case MOE_W_INT4_U4B8: return launch_gemm_int4(small, stage, bn, g, grid, st);
     case MOE_W_MXFP4: return launch_gemm_mxfp4(small, stage, bn, g, grid, st);
     case MOE_W_NVFP4: return launch_gemm_nvfp4(small, stage, bn, g, grid, st);
+    case kFmtInt4X: return launch_gemm_int4x(small, stage, bn, g, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -269,8 +271,9 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   // token, the tcgen05 kernel reads them in sorted order; GEMM2 reads GEMM1's
   // fp16 output in sorted order
   CUtensorMap map2;
-  if (small ? !make_gather_map(&g.tmap_b, ws + w.xh_off, L.K, M)
-            : !make_act_map3(&g.tmap_b, ws + w.xh_off, L.K, w.cap, bn, kSup))
+  const bool gather_rows = small && !L.act_order;  // else x's routed rows in sorted order
+  if (gather_rows ? !make_gather_map(&g.tmap_b, ws + w.xh_off, L.K, M)
+                  : !make_act_map3(&g.tmap_b, ws + w.xh_off, L.K, w.cap, bn, small ? kSmallChunk : kSup))
     return MOE_ERR_CUDA;
   if (!make_act_map3(&map2, ws + w.a_off, L.Npad, w.cap, bn, small ? kSmallChunk : kSup)) return MOE_ERR_CUDA;
 
@@ -309,14 +312,18 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
     if (!small) pa.align_ctas = align_copy_ctas(M * top_k, L.K, w.grid);
   } else {
     pa.given_sorted = sorted_ids;
+    pa.given_expert_ids = expert_ids;
     pa.given_n_padded = n_padded;
+    pa.block_m = block_m;
+    pa.E = L.E;
   }
   pa.x = static_cast<const uint16_t*>(x);
   pa.M = M;
   pa.K = L.K;
   pa.top_k = top_k;
-  if (small) pa.xh = reinterpret_cast<uint16_t*>(ws + w.xh_off);
+  if (gather_rows) pa.xh = reinterpret_cast<uint16_t*>(ws + w.xh_off);
   else pa.xs = reinterpret_cast<uint16_t*>(ws + w.xh_off);
+  if (L.act_order) pa.perm13 = reinterpret_cast<const int32_t*>(pk + L.perm13_off);
   pa.zero = reinterpret_cast<uint32_t*>(ws);
   pa.zero_words = w.header_bytes / 4;
   if (launch_prologue(pa, w.grid, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -331,6 +338,8 @@ static int forward_impl(const moe_layer_desc* desc, const Layout& L, const WsPla
   g.pairs = M * top_k;
   g.top_k = top_k;
   g.align_early = (own_align && !split_align) ? 0 : 1;
+  g.zp_float = L.zero_kind == 2;
+  g.gemm1_rows_sorted = gather_rows ? 0 : 1;
   g.block_m = block_m;
   g.act_kind = act;
   g.alpha = alpha;

@@ -42,6 +42,14 @@ namespace moe {
 // Scales ride in front of the stage that first needs them: INT4 (one bf16 per
 // 128 = two stages) only in front of even stages, 256 x bf16; MXFP4 two E8M0
 // bytes per row per stage (256 x u16); NVFP4 four E4M3 bytes (256 x u32).
+//
+// INT4 banks with zero points or groups of 32 / 64 are packed as INT4X: one
+// 32-bit entry per row and 32-element half stage, two f16 -- the multiplier m
+// (the scale) and x: 1024 + z for integer zero points (1032 without), or
+// -z * m for float zero points -- 256 x 2 x u32 in front of every stage.
+// Act-order banks store each expert matrix's reduction dimension in
+// sort_indices order (groups contiguous) and keep w13's permutation for the
+// forward, which applies it to x's columns.
 // ----------------------------------------------------------------------------
 constexpr int kTileRows = 256;       // weight rows per CTA tile (2 x 128)
 constexpr int kStageK = 64;          // reduction elements per stage
@@ -54,8 +62,14 @@ enum GemmStage : int {
   kGemm1Relu2 = 2,  // a = relu(h)^2, non-gated experts, fp16
 };
 
+// Packed format of INT4 banks with zero points or groups below 128 (internal;
+// the public enum has the checkpoint formats).
+constexpr int kFmtInt4X = 3;
+
 struct Layout {
-  int fmt, E, K, N, group;
+  int fmt, E, K, N, group;  // fmt: the packed format (MOE_W_* or kFmtInt4X); group as given (-1: per row)
+  int zero_kind;   // INT4: 0 none, 1 integer, 2 float zero points
+  int act_order;   // INT4: reduction dims stored in sort_indices order
   int gated;       // 1: GEMM1 tiles pair 128 gate rows with their 128 up rows; 0: 256 rows of h
   int Npad;        // roundup(N, 128) gated, roundup(N, 256) non-gated
   int Kpad2;       // roundup(K, 256)
@@ -65,19 +79,28 @@ struct Layout {
   int scale_bytes; // scale bytes per chunk
   int64_t period_bytes;   // scale_bytes + period * 8192
   int64_t tile1_bytes, tile2_bytes;
-  int64_t w13_off, w2_off, b13_off, b2_off, gs13_off, gs2_off, shift_off, total;
+  int64_t w13_off, w2_off, b13_off, b2_off, gs13_off, gs2_off, shift_off, perm13_off, total;
 };
 
 __host__ __device__ inline int64_t round_up64(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
 __host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
   if (d.fmt < 0 || d.fmt > 2 || d.num_experts <= 0 || d.hidden <= 0 || d.inter <= 0) return false;
-  const int want_group = d.fmt == MOE_W_INT4_U4B8 ? 128 : (d.fmt == MOE_W_MXFP4 ? 32 : 16);
-  if (d.group_size != want_group) return false;
-  if (d.hidden % 64 || d.inter % d.group_size) return false;
-  if (d.fmt == MOE_W_INT4_U4B8 && d.hidden % 128) return false;
+  const bool int4 = d.fmt == MOE_W_INT4_U4B8;
+  if (int4) {
+    const int g = d.group_size;
+    if (g != 32 && g != 64 && g != 128 && g != -1) return false;
+    if (d.zero_kind < 0 || d.zero_kind > 2 || (d.act_order != 0 && d.act_order != 1)) return false;
+    if (d.act_order && g < 0) return false;  // act-order groups have a size
+    if (d.hidden % 128 || (g > 0 && d.inter % g)) return false;
+  } else {
+    if (d.group_size != (d.fmt == MOE_W_MXFP4 ? 32 : 16) || d.zero_kind || d.act_order) return false;
+    if (d.hidden % 64 || d.inter % d.group_size) return false;
+  }
   if (d.non_gated != 0 && (d.non_gated != 1 || d.w13_interleaved)) return false;
-  L->fmt = d.fmt;
+  L->fmt = (int4 && (d.zero_kind != 0 || (d.group_size > 0 && d.group_size < 128))) ? kFmtInt4X : d.fmt;
+  L->zero_kind = int4 ? d.zero_kind : 0;
+  L->act_order = int4 ? d.act_order : 0;
   L->E = d.num_experts;
   L->K = d.hidden;
   L->N = d.inter;
@@ -90,8 +113,8 @@ __host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
   L->T2 = L->Kpad2 / 256;
   L->S1 = d.hidden / kStageK;
   L->S2 = L->Npad / kStageK;
-  L->period = d.fmt == MOE_W_INT4_U4B8 ? 2 : 1;
-  L->scale_bytes = kTileRows * (d.fmt == MOE_W_NVFP4 ? 4 : 2);
+  L->period = L->fmt == MOE_W_INT4_U4B8 ? 2 : 1;
+  L->scale_bytes = kTileRows * (L->fmt == kFmtInt4X ? 8 : (L->fmt == MOE_W_NVFP4 ? 4 : 2));
   L->period_bytes = L->scale_bytes + (int64_t)L->period * kPackedStageBytes;
   L->tile1_bytes = (int64_t)(L->S1 / L->period) * L->period_bytes;
   L->tile2_bytes = (int64_t)(L->S2 / L->period) * L->period_bytes;
@@ -110,6 +133,8 @@ __host__ inline bool make_layout(const moe_layer_desc& d, Layout* L) {
   off += (int64_t)L->E * 4;
   L->shift_off = off = round_up64(off, 256);  // int32 [2][E]: scale exponent shift of w13 and w2
   off += (int64_t)2 * L->E * 4;
+  L->perm13_off = off = round_up64(off, 256);  // act-order: int32 [E][K], x column of packed column k
+  if (L->act_order) off += (int64_t)L->E * L->K * 4;
   L->total = round_up64(off, 256);
   return true;
 }
@@ -127,7 +152,9 @@ __host__ __device__ inline bool stage_has_scales(const Layout& L, int s) { retur
 template <int FMT>
 struct PackedFmt {
   static constexpr int kPeriod = FMT == MOE_W_INT4_U4B8 ? 2 : 1;
-  static constexpr int kScaleBytes = kTileRows * (FMT == MOE_W_NVFP4 ? 4 : 2);
+  static constexpr int kScaleBytes = kTileRows * (FMT == kFmtInt4X ? 8 : (FMT == MOE_W_NVFP4 ? 4 : 2));
+  static constexpr int kMaxScaleBytesPerStage = FMT == kFmtInt4X ? 2048 : 1024;  // ring slot sizing
+  static constexpr int kSlotBytes(int stages) { return stages * (kPackedStageBytes + kMaxScaleBytesPerStage); }
   static constexpr int kPeriodBytes = kScaleBytes + kPeriod * kPackedStageBytes;
   __host__ __device__ static constexpr int stage_off(int ss) {
     return (ss / kPeriod) * kPeriodBytes + (ss % kPeriod ? kScaleBytes + (ss % kPeriod) * kPackedStageBytes : 0);
@@ -160,7 +187,9 @@ constexpr int kE8m0Min = 112, kE8m0Max = 148;
 
 // Packed-blob header (its first 256 bytes): word 0 holds these flags.
 constexpr uint32_t kFlagInt4Window = 1u;  // an INT4 scale outside the fp16 window (tcgen05 path only)
-constexpr uint32_t kFlagFp4Window = 2u;   // an MXFP4 scale byte outside the fp16 window (both GEMM paths)
+constexpr uint32_t kFlagFp16Window = 2u;  // an MXFP4 scale byte, or an INT4 scale of a zero-point /
+                                          // small-group bank, outside the fp16 window (both GEMM paths)
+constexpr uint32_t kFlagGroups = 4u;      // act-order groups that are not group_size indices each
 
 // ----------------------------------------------------------------------------
 // Device status word (first 4 bytes of the forward workspace).
@@ -510,6 +539,46 @@ __device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t m01, uint32_t m2
   for (int i = 0; i < 4; ++i) {
     const uint32_t m = i < 2 ? m01 : m23;
     const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&v[i]), *reinterpret_cast<const __half2*>(&m));
+    o[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+// 8 INT4 codes of one word with a zero point, from a 32-element half stage's
+// entry: low-nibble pairs (1024 + q) - c_lo, high-nibble pairs (1024 + 16q) -
+// c_hi, then times m (m / 16 for the high pairs) plus o, in one fused op.  For
+// integer zero points c_lo = 1024 + z, c_hi = 1024 + 16z, o = 0 (q - z exact,
+// one rounding of (q - z) * m); for float zero points c = 1024 and o = -z * m.
+struct Int4ZpConst {
+  uint32_t c_lo, c_hi, m, m16, o;  // f16x2 (both halves equal)
+};
+__device__ __forceinline__ Int4ZpConst int4zp_const(uint32_t entry, int zp_float) {
+  const uint32_t m = entry & 0xFFFFu, x = entry >> 16;
+  const __half one024 = __ushort_as_half(0x6400);
+  const __half hx = __ushort_as_half((uint16_t)x);
+  // c_hi = 16 c_lo - 15360 = 1024 + 16 z (exact)
+  const __half chi = __hsub(__hmul(hx, __ushort_as_half(0x4C00)), __ushort_as_half(0x7380));
+  const uint16_t clo_b = zp_float ? (uint16_t)0x6400 : (uint16_t)x;
+  const uint16_t chi_b = zp_float ? (uint16_t)0x6400 : __half_as_ushort(chi);
+  const uint16_t o_b = zp_float ? (uint16_t)x : (uint16_t)0;
+  const uint16_t m16_b = __half_as_ushort(__hmul(__ushort_as_half((uint16_t)m), __ushort_as_half(0x2C00)));
+  (void)one024;
+  Int4ZpConst k;
+  k.c_lo = (uint32_t)clo_b | ((uint32_t)clo_b << 16);
+  k.c_hi = (uint32_t)chi_b | ((uint32_t)chi_b << 16);
+  k.m = m | (m << 16);
+  k.m16 = (uint32_t)m16_b | ((uint32_t)m16_b << 16);
+  k.o = (uint32_t)o_b | ((uint32_t)o_b << 16);
+  return k;
+}
+__device__ __forceinline__ void int4x8_f16_zp(uint32_t w, const Int4ZpConst& k, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t t[4] = {(w & 0x000F000Fu) | 0x64006400u, (w & 0x00F000F0u) | 0x64006400u,
+                         (w8 & 0x000F000Fu) | 0x64006400u, (w8 & 0x00F000F0u) | 0x64006400u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = (i & 1) ? k.c_hi : k.c_lo, m = (i & 1) ? k.m16 : k.m;
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t[i]), *reinterpret_cast<const __half2*>(&c));
+    const __half2 r = __hfma2(v, *reinterpret_cast<const __half2*>(&m), *reinterpret_cast<const __half2*>(&k.o));
     o[i] = *reinterpret_cast<const uint32_t*>(&r);
   }
 }

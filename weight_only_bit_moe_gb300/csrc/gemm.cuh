@@ -51,7 +51,6 @@ constexpr int kEpiThreads = kNumEpiWarps * 32;
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpBProducer = 2, kWarpDequant0 = 3;
 constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..18
 constexpr int kGemmThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 608
-constexpr int kPackedSlotBytes = kSup * (kPackedStageBytes + 1024);  // a unit's codes + largest scale blocks
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint32_t kTmemCols = 512;                         // whole TMEM (one CTA per SM)
 constexpr uint32_t kAColsPerStage = 64;                     // 2 halves x 64 K / 2 per column
@@ -84,10 +83,13 @@ struct GemmArgs {
   int32_t* counters;          // split-K arrival counters [T * blocks]
   unsigned* status;
   int test_starve_wait;       // test hook (register-fed kernel): CTA 0 ends with a wait nothing completes
+  int zp_float;               // INT4X: entries carry -z * m (float zero points) instead of 1024 + z
+  int gemm1_rows_sorted;      // register-fed GEMM1: read x's routed rows in sorted order (act-order banks)
 };
 
-template <int BN>
+template <int BN, int FMT>
 struct GemmSmem {
+  static constexpr int kPackedSlotBytes = PackedFmt<FMT>::kSlotBytes(kSup);  // a unit's codes + scale blocks
   static constexpr int kSA = 2;                    // dequantised-A ring in TMEM, in units
   static constexpr int kNacc = BN >= 128 ? 1 : 2;  // TMEM accumulators
   static constexpr int kBUnitBytes = kSup * BN * 128;  // activation rows of a unit, [stage][row][64]
@@ -216,8 +218,8 @@ __device__ __forceinline__ bool live_sid(int sid, int pairs) { return (unsigned)
 // Header flags of the packed blob that make a kernel's fp16 operands inexact:
 // the tcgen05 path dequantises INT4 with fp16 scales, the register-fed path
 // applies INT4 scales in fp32; both turn MXFP4 scales into fp16 multipliers.
-constexpr uint32_t kStatusBlobFlagsTc = kFlagInt4Window | kFlagFp4Window;
-constexpr uint32_t kStatusBlobFlagsSmall = kFlagFp4Window;
+constexpr uint32_t kStatusBlobFlagsTc = kFlagInt4Window | kFlagFp16Window | kFlagGroups;
+constexpr uint32_t kStatusBlobFlagsSmall = kFlagFp16Window | kFlagGroups;
 
 // End-of-kernel status of one epilogue thread (after its dependency wait): an
 // fp16 value that overflowed (|v| >= 65520 rounds to infinity) or is not a
@@ -311,7 +313,8 @@ template <int FMT, int STAGE, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
   constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
   constexpr bool kGated = STAGE == kGemm1Gated;  // tile halves are gate and up rows
-  using SM = GemmSmem<BN>;
+  using SM = GemmSmem<BN, FMT>;
+  constexpr int kPackedSlotBytes = SM::kPackedSlotBytes;
   using PF = PackedFmt<FMT>;
   constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc, kSA = SM::kSA;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -508,6 +511,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
               m[j][0] = a | (a << 16);
               m[j][1] = c | (c << 16);
+            } else if (FMT == kFmtInt4X) {  // the row's entries of both 32-element halves
+              const uint2 ev = lds64(st + 8 * r);
+              m[j][0] = ev.x;
+              m[j][1] = ev.y;
             } else {
               const uint32_t sv = lds32(st + 4 * r);
               const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
@@ -531,17 +538,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             const uint32_t wd[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
                                     u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
             uint32_t o[32];  // TMEM column c = K pair (2c, 2c+1) of the stage
+            if (FMT == kFmtInt4X) {
+              // words of one 32-element half share its entry: h outer
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
-              // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
-              const int t = v >> 1, h = v & 1;
-              uint32_t t4[4];
-              if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[j][0], m[j][1], t4);
-              else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[j][h], m[j][h], t4);
-              else e2m1x8_f16(wd[v], m[j][2 * h], m[j][2 * h + 1], t4);
+              for (int h = 0; h < 2; ++h) {
+                const Int4ZpConst kc = int4zp_const(m[j][h], g.zp_float);
 #pragma unroll
-              for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
+                for (int t = 0; t < 4; ++t) {
+                  uint32_t t4[4];
+                  int4x8_f16_zp(wd[2 * t + h], kc, t4);
+#pragma unroll
+                  for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
+                }
+              }
+            } else {
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
+                // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
+                const int t = v >> 1, h = v & 1;
+                uint32_t t4[4];
+                if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[j][0], m[j][1], t4);
+                else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[j][h], m[j][h], t4);
+                else e2m1x8_f16(wd[v], m[j][2 * h], m[j][2 * h + 1], t4);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
+              }
             }
             if (j == 0) {
               mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);

@@ -18,11 +18,11 @@ cudaError_t launch_gemm_instance(const GemmArgs& g, int grid, cudaStream_t st) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     err = cudaFuncSetAttribute(moe_gemm_kernel<FMT, STAGE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               GemmSmem<BN>::kAlloc);
+                               GemmSmem<BN, FMT>::kAlloc);
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
-  return launch_dependent(moe_gemm_kernel<FMT, STAGE, BN>, dim3(grid), dim3(kGemmThreads), GemmSmem<BN>::kAlloc, st, g);
+  return launch_dependent(moe_gemm_kernel<FMT, STAGE, BN>, dim3(grid), dim3(kGemmThreads), GemmSmem<BN, FMT>::kAlloc, st, g);
 }
 
 template <int FMT, int BN>
@@ -54,12 +54,12 @@ cudaError_t launch_gemm_small_instance(const GemmArgs& g, int grid, cudaStream_t
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     err = cudaFuncSetAttribute(moe_gemm_small_kernel<FMT, STAGE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SmallSmem<BN>::kAlloc);
+                               SmallSmem<BN, FMT>::kAlloc);
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
   return launch_dependent(moe_gemm_small_kernel<FMT, STAGE, BN>, dim3(grid), dim3(kSmallThreads),
-                          SmallSmem<BN>::kAlloc, st, g);
+                          SmallSmem<BN, FMT>::kAlloc, st, g);
 }
 
 template <int FMT, int BN>
@@ -87,5 +87,6 @@ cudaError_t launch_gemm_small_fmt(int stage, int bn, const GemmArgs& g, int grid
 cudaError_t launch_gemm_int4(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st);
 cudaError_t launch_gemm_mxfp4(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st);
 cudaError_t launch_gemm_nvfp4(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st);
+cudaError_t launch_gemm_int4x(bool small, int stage, int bn, const GemmArgs& g, int grid, cudaStream_t st);
 
 }  // namespace moe

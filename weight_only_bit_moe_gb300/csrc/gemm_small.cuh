@@ -38,12 +38,12 @@ constexpr int kSmallChunk = 4;  // 64-K stages per TMA chunk
 constexpr int kSmallConsumerWarps = 8;
 constexpr int kSmallMI = kTileRows / 16 / kSmallConsumerWarps;  // 16-row fragments per consumer warp
 constexpr int kSmallThreads = (1 + kSmallConsumerWarps) * 32;
-constexpr int kSmallWBytes = kSmallChunk * (kPackedStageBytes + 1024);  // codes + largest scale block
 
-template <int BN>
+template <int BN, int FMT>
 struct SmallSmem {
+  static constexpr int kWBytes = PackedFmt<FMT>::kSlotBytes(kSmallChunk);  // codes + scale blocks of a chunk
   static constexpr int kBBytes = kSmallChunk * BN * 128;  // activation rows of a chunk, [stage][row][64]
-  static constexpr int kSlotBytes = kSmallWBytes + kBBytes;
+  static constexpr int kSlotBytes = kWBytes + kBBytes;
   static constexpr int kFit = (kSmemBudget - 2048) / kSlotBytes;
   static constexpr int kSlots = kFit > 6 ? 6 : kFit;
   static constexpr int kBar = kSlots * kSlotBytes;
@@ -53,7 +53,7 @@ struct SmallSmem {
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kSlots >= 4, "ring too shallow");
   static_assert(kAlloc <= 232448, "shared memory over the per-CTA limit");
-  static_assert(kBBytes % 1024 == 0 && kSmallWBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+  static_assert(kBBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
 };
 
 // Split-K choice in units of 1/8 stage: each wave streams ceil(units/S)
@@ -150,7 +150,8 @@ __device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT>& F
 // codes in fp16 (exact).
 template <int FMT, int NT, int BN, int NST>
 __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const SmallFrag<NT>& F,
-                                              float (&acc)[kSmallMI][NT][4], uint32_t (&m)[kSmallMI][2][4]) {
+                                              float (&acc)[kSmallMI][NT][4], uint32_t (&m)[kSmallMI][2][4],
+                                              int zp_float) {
   using PF = PackedFmt<FMT>;
   if constexpr (FMT == MOE_W_INT4_U4B8) {
 #pragma unroll
@@ -198,6 +199,37 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[i][n][c] = fmaf(sc[i][c >> 1], part[i][n][c], acc[i][n][c]);
     }
+  } else if constexpr (FMT == kFmtInt4X) {
+    // one 32-bit entry (multiplier, zero term) per row and 32-element half stage;
+    // codes dequantised to fp16 with it (as the tcgen05 kernel does)
+#pragma unroll
+    for (int ss = 0; ss < NST; ++ss) {
+      uint2 ev[kSmallMI][2];
+#pragma unroll
+      for (int i = 0; i < kSmallMI; ++i)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) ev[i][hr] = lds64(wsl + PF::stage_off(ss) + F.sc_off[i][hr]);
+      uint2 wv[kSmallMI][2];
+#pragma unroll
+      for (int i = 0; i < kSmallMI; ++i)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) wv[i][hr] = lds64(wsl + PF::codes_off(ss) + F.code_off[i][hr]);
+      uint32_t bf[4][NT][2];
+      load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
+#pragma unroll
+      for (int i = 0; i < kSmallMI; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t p0[4], p1[4];  // fragment rows gq and gq + 8, K half h
+          int4x8_f16_zp(h ? wv[i][0].y : wv[i][0].x, int4zp_const(h ? ev[i][0].y : ev[i][0].x, zp_float), p0);
+          int4x8_f16_zp(h ? wv[i][1].y : wv[i][1].x, int4zp_const(h ? ev[i][1].y : ev[i][1].x, zp_float), p1);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            mma_16816(acc[i][n], p0[0], p1[0], p0[1], p1[1], bf[2 * h][n][0], bf[2 * h][n][1]);
+            mma_16816(acc[i][n], p0[2], p1[2], p0[3], p1[3], bf[2 * h + 1][n][0], bf[2 * h + 1][n][1]);
+          }
+        }
+    }
   } else {
 #pragma unroll
     for (int ss = 0; ss < NST; ++ss) {
@@ -241,7 +273,8 @@ template <int FMT, int STAGE, int BN>
 __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const __grid_constant__ GemmArgs g) {
   constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
   constexpr bool kGated = STAGE == kGemm1Gated;  // fragment rows pair gate and up features
-  using SM = SmallSmem<BN>;
+  using SM = SmallSmem<BN, FMT>;
+  constexpr int kSmallWBytes = SM::kWBytes;
   constexpr int kSlots = SM::kSlots;
   constexpr int NT = BN / 8;  // 8-token column tiles
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -297,10 +330,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     uint32_t npend = 0;
     bool waited = !g.align_early;
     uint32_t ck = 0;
+    // GEMM1 gathers token rows, unless the prologue placed them in sorted order
+    // (act-order banks, whose x columns follow each expert's order)
+    const bool gather = kG1 && !g.gemm1_rows_sorted;
     // activation copies of chunk `stage0` (nst stages) into slot `slot`, rows from `rows`
     auto issue_act = [&](int slot, int row0, int stage0, int nst, const int32_t* rows) {
       const uint32_t dst = smem_u32(smem + slot * SM::kSlotBytes + kSmallWBytes);
-      if (kG1) {
+      if (gather) {
         const uint32_t rows_s = smem_u32(rows);
         for (int q = lane; q < nst * (BN / 4); q += 32) {
           const int j = q / (BN / 4), r4 = q % (BN / 4);
@@ -318,7 +354,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       stage_range(plan, L, split, s0, s1);
       const int e = block_expert(g, b);
       if (e < 0) continue;  // (the consumers skip it too)
-      if (kG1) {
+      if (gather) {
         __syncwarp();  // the previous item's rows are consumed
         load_block_rows(g, b, BN, lane, item_rows);
         __syncwarp();
@@ -336,7 +372,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         // c0 and c1 lie on scale-period boundaries
         const int64_t off0 = (int64_t)(c0 / PackedFmt<FMT>::kPeriod) * PackedFmt<FMT>::kPeriodBytes;
         const uint32_t wbytes = (uint32_t)((c1 - c0) / PackedFmt<FMT>::kPeriod * PackedFmt<FMT>::kPeriodBytes);
-        const uint32_t bbytes = kG1 ? (uint32_t)((c1 - c0) * BN * 128) : (uint32_t)SM::kBBytes;
+        const uint32_t bbytes = gather ? (uint32_t)((c1 - c0) * BN * 128) : (uint32_t)SM::kBBytes;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[slot], wbytes + bbytes);
           bulk_g2s(smem + slot * SM::kSlotBytes, tb + off0, wbytes, &full[slot], pol);
@@ -345,7 +381,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         if (waited) {
           issue_act(slot, b * g.block_m, c0, c1 - c0, item_rows);
         } else {  // ck < kSlots: slot == ck
-          if (kG1 && lane < BN) pend_rows[32 * npend + lane] = item_rows[lane];
+          if (gather && lane < BN) pend_rows[32 * npend + lane] = item_rows[lane];
           pend_row[npend] = b * g.block_m;
           pend_stage[npend] = c0;
           pend_nst[npend] = c1 - c0;
@@ -387,7 +423,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         F.code_off[i][h] = (uint32_t)(((tq >> 1) * 256 + rows[i][h]) * 16 + (tq & 1) * 8);
-        F.sc_off[i][h] = (uint32_t)(rows[i][h] * (FMT == MOE_W_NVFP4 ? 4 : 2));
+        F.sc_off[i][h] = (uint32_t)(rows[i][h] * (FMT == kFmtInt4X ? 8 : (FMT == MOE_W_NVFP4 ? 4 : 2)));
       }
     // ldmatrix row addresses: token row n, 16-byte chunk c of a stage block sits
     // at n * 128 + ((c ^ (n & 7)) << 4) (the TMA's 128-byte swizzle)
@@ -436,11 +472,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         const uint32_t wsl = smem_u32(smem + slot * SM::kSlotBytes);
         const uint32_t bsl = wsl + kSmallWBytes;
         const int nst = min(kSmallChunk, s1 - c0);
-        if (nst == 4) consume_chunk<FMT, NT, BN, 4>(wsl, bsl, F, acc, m);
-        else if (nst == 2) consume_chunk<FMT, NT, BN, 2>(wsl, bsl, F, acc, m);
+        if (nst == 4) consume_chunk<FMT, NT, BN, 4>(wsl, bsl, F, acc, m, g.zp_float);
+        else if (nst == 2) consume_chunk<FMT, NT, BN, 2>(wsl, bsl, F, acc, m, g.zp_float);
         else if (FMT != MOE_W_INT4_U4B8) {  // INT4 chunks always hold whole 2-stage periods
-          if (nst == 3) consume_chunk<FMT, NT, BN, 3>(wsl, bsl, F, acc, m);
-          else consume_chunk<FMT, NT, BN, 1>(wsl, bsl, F, acc, m);
+          if (nst == 3) consume_chunk<FMT, NT, BN, 3>(wsl, bsl, F, acc, m, g.zp_float);
+          else consume_chunk<FMT, NT, BN, 1>(wsl, bsl, F, acc, m, g.zp_float);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);

@@ -23,7 +23,10 @@ struct PrologueArgs {
                              // (tcgen05 GEMMs), or NULL; written as this launch aligns, or else from
                              // the caller's alignment below (padding rows are not written)
   const int32_t* given_sorted;   // the caller's alignment (moe_align), read when this launch does not align
+  const int32_t* given_expert_ids;
   const int32_t* given_n_padded;
+  const int32_t* perm13;     // act-order banks: int32 [E][K], x column of packed column k of expert e
+                             // (xs rows then hold x's columns in their expert's order), or NULL
   int32_t* pair_pos;         // [pairs] scratch: sorted position of each local pair (xs while aligning)
   int align_ctas;            // CTAs that align (and copy their pairs' rows); 0: the minimum
   // workspace header words to clear (zero_words == 0: none)

@@ -21,6 +21,7 @@ from . import binding as B
 FMT = {"int4": B.MOE_W_INT4_U4B8, "mxfp4": B.MOE_W_MXFP4, "nvfp4": B.MOE_W_NVFP4}
 ACT = {"silu_mul": B.MOE_ACT_SILU_MUL, "sigmoid_alpha": B.MOE_ACT_SIGMOID_ALPHA, "relu2": B.MOE_ACT_RELU2}
 GROUP = {"int4": 128, "mxfp4": 32, "nvfp4": 16}
+ZERO_KIND = {"": 0, "int": 1, "float": 2}
 
 
 def _dev(a: Optional[np.ndarray], device, dtype=None) -> Optional[torch.Tensor]:
@@ -48,16 +49,25 @@ class MoELayer:
     """One layer's expert bank on one GPU, repacked for the kernels."""
 
     def __init__(self, fmt: str, num_experts: int, hidden: int, inter: int, w13, w13_s, w13_gs, b13, w2, w2_s,
-                 w2_gs, b2, interleaved: bool = False, gated: bool = True, stream=None):
+                 w2_gs, b2, interleaved: bool = False, gated: bool = True, group_size: int = 0,
+                 zero_kind: str = "", w13_zeros=None, w2_zeros=None, w13_g_idx=None, w2_g_idx=None,
+                 w13_sort_indices=None, w2_sort_indices=None, stream=None):
+        """group_size 0: the format's own; INT4 variants: zero_kind "int" / "float" with
+        w*_zeros, act-order with w*_g_idx and w*_sort_indices, group_size 32/64/128/-1."""
         self.fmt = fmt
         self.E, self.K, self.N = num_experts, hidden, inter
         self.gated = gated  # False: w13 holds N rows and the activation is relu2
-        self.desc = B.moe_layer_desc(FMT[fmt], num_experts, hidden, inter, GROUP[fmt], int(interleaved),
-                                     int(b13 is not None), int(b2 is not None), int(not gated))
+        act_order = w13_g_idx is not None
+        self.desc = B.moe_layer_desc(FMT[fmt], num_experts, hidden, inter, group_size or GROUP[fmt],
+                                     int(interleaved), int(b13 is not None), int(b2 is not None), int(not gated),
+                                     ZERO_KIND[zero_kind], int(act_order))
         dev = w13.device
         self.device = dev
         self.packed = torch.empty(B.moe_repack_size(self.desc), dtype=torch.uint8, device=dev)
-        B.moe_repack_weights(self.desc, w13, w13_s, w13_gs, b13, w2, w2_s, w2_gs, b2, self.packed, stream)
+        B.moe_repack_weights_ex(self.desc, dict(
+            w13=w13, w13_s=w13_s, w13_gs=w13_gs, b13=b13, w13_zeros=w13_zeros, w13_g_idx=w13_g_idx,
+            w13_sort_indices=w13_sort_indices, w2=w2, w2_s=w2_s, w2_gs=w2_gs, b2=b2, w2_zeros=w2_zeros,
+            w2_g_idx=w2_g_idx, w2_sort_indices=w2_sort_indices), self.packed, stream)
         self._ws = {}
 
     @classmethod
@@ -65,8 +75,14 @@ class MoELayer:
         """W: a workloads.LayerWeights (host arrays in checkpoint layout)."""
         t = dict(w13=_dev(W.w13, device), w13_s=_dev(W.w13_s, device), w13_gs=_dev(W.w13_gs, device),
                  b13=_dev(W.b13, device), w2=_dev(W.w2, device), w2_s=_dev(W.w2_s, device),
-                 w2_gs=_dev(W.w2_gs, device), b2=_dev(W.b2, device))
-        layer = cls(W.fmt, W.E, W.K, W.N, interleaved=W.interleaved, gated=W.gated, stream=stream, **t)
+                 w2_gs=_dev(W.w2_gs, device), b2=_dev(W.b2, device),
+                 w13_zeros=_dev(getattr(W, "w13_z", None), device), w2_zeros=_dev(getattr(W, "w2_z", None), device),
+                 w13_g_idx=_dev(getattr(W, "w13_gidx", None), device),
+                 w2_g_idx=_dev(getattr(W, "w2_gidx", None), device),
+                 w13_sort_indices=_dev(getattr(W, "w13_perm", None), device),
+                 w2_sort_indices=_dev(getattr(W, "w2_perm", None), device))
+        layer = cls(W.fmt, W.E, W.K, W.N, interleaved=W.interleaved, gated=W.gated, group_size=W.group,
+                    zero_kind=getattr(W, "zero_kind", ""), stream=stream, **t)
         torch.cuda.current_stream(device).synchronize()  # source tensors may be freed after this
         return layer
 
