@@ -68,6 +68,9 @@ __device__ __forceinline__ WorkPlan make_plan_small(const GemmArgs& g, bool gemm
   const int base = p.T * p.nb;
   const int grid = (int)gridDim.x;
   int S = 1;
+  // (Only below one wave: a second, partly filled wave of whole items measured
+  // faster on GB300 than more waves of split ones -- the streaming SMs of a
+  // partial wave take a larger share of HBM.)
   if (base > 0 && base < grid && p.nb * g.block_m <= g.split_rows) {
     const int per = g.L.period * 8;
     int best = p.units * per;
