@@ -156,26 +156,6 @@ __device__ __forceinline__ uint4 transpose8x8_u16(const uint32_t (&w)[4], int la
   return b2 ? make_uint4(rc, rd, x10, x11) : make_uint4(x00, x01, rc, rd);
 }
 
-// The same transpose for 32-bit values: on entry lane L holds feature L's
-// values of tokens 0..7 in v[0..7]; on exit v[j] holds feature (L & ~7) + j of
-// token L & 7.  Three butterfly steps (lane bit i <-> register bit i), four
-// shuffles each.
-__device__ __forceinline__ void transpose8x8_u32(float (&v)[8], int lane) {
-#pragma unroll
-  for (int i = 0; i < 3; ++i) {
-    const int m = 1 << i;
-    const bool up = (lane >> i) & 1;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j & m) continue;
-      const float send = up ? v[j] : v[j | m];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, m);
-      if (up) v[j] = recv;
-      else v[j | m] = recv;
-    }
-  }
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
@@ -745,40 +725,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               stg128(dst + 128, o1);
             }
           } else {
-            // fp32 rows by pair, transposed: each lane stores 8 consecutive
-            // outputs of one pair per half (two 16-byte stores); ok0/ok1 are
-            // warp-uniform (K % 64 == 0 and a warp's 32 rows start on a multiple
-            // of 32).  Padding columns are stored by no lane.
-            const int tt = lane & 7;
-            const int sid_t = epi_sid[c0 + tt];
-            const bool live = c0 + tt < jmax && live_sid(sid_t, g.pairs);
-            float* dst = g.y_out + (int64_t)(live ? sid_t : 0) * L.K + (row0 - hr) + q * 32 + (lane & 24);
-            // y is fp32: only a non-finite value of a live column is an error
-            // (NaN, or an infinity from an overflow upstream)
-            if (ok0) {
-              float v[8];
+            // fp32 rows by pair: for each token column the warp's 32 lanes hold 32
+            // consecutive outputs of one pair, one 128-byte store per half; the
+            // column test and ok0/ok1 are warp-uniform (K % 64 == 0 and a warp's
+            // 32 rows start on a multiple of 32).  Padding columns are stored by
+            // no lane.  y is fp32: only a non-finite value of a live column is an
+            // error (NaN, or an infinity from an overflow upstream).
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                v[j] = f0[j] * gsc + bias0;
-                if (live_sid(sid[j], g.pairs)) vmax = fmax_nan(vmax, v[j] * 0.0f);
-              }
-              transpose8x8_u32(v, lane);
-              if (live) {
-                stg128(dst, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3])));
-                stg128(dst + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]), __float_as_uint(v[7])));
-              }
-            }
-            if (ok1) {
-              float v[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                v[j] = f1[j] * gsc + bias1;
-                if (live_sid(sid[j], g.pairs)) vmax = fmax_nan(vmax, v[j] * 0.0f);
-              }
-              transpose8x8_u32(v, lane);
-              if (live) {
-                stg128(dst + 128, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3])));
-                stg128(dst + 132, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]), __float_as_uint(v[7])));
+            for (int j = 0; j < 8; ++j) {
+              if (c0 + j < jmax && live_sid(sid[j], g.pairs)) {
+                float* dst = g.y_out + (int64_t)sid[j] * L.K + row0;
+                if (ok0) {
+                  const float v = f0[j] * gsc + bias0;
+                  vmax = fmax_nan(vmax, v * 0.0f);
+                  dst[0] = v;
+                }
+                if (ok1) {
+                  const float v = f1[j] * gsc + bias1;
+                  vmax = fmax_nan(vmax, v * 0.0f);
+                  dst[128] = v;
+                }
               }
             }
           }
