@@ -587,12 +587,18 @@ __device__ __forceinline__ void int4x8_f16_zp(uint32_t w, const Int4ZpConst& k, 
 __device__ __forceinline__ uint32_t bf16_scale_f16(uint32_t sbits) {
   return __half_as_ushort(__float2half_rn(__uint_as_float(sbits << 16)));
 }
-// E8M0 byte b -> 2^(b-127) * 2^-8 = 2^(b-135) as fp16 (normal for b >= 121,
-// subnormal power of two for 111 <= b <= 120, 0 below; 255 is NaN).  Bytes
-// above 150 do not occur: the repack shift keeps them in [112, 148].
-__device__ __forceinline__ uint32_t e8m0_mult_f16(uint32_t b) {
-  if (b == 255u) return 0x7E00u;
-  return b >= 121u ? (((b - 120u) & 0x1Fu) << 10) : (b >= 111u ? (1u << (b - 111u)) : 0u);
+// Two E8M0 bytes (low = first) -> f16x2 of 2^(b-127) * 2^-8 = 2^(b-135) each:
+// normal for b >= 121, a subnormal power of two for 111 <= b <= 120, 0 below
+// (the conversion rounds to nearest even); 255 is NaN.  Bytes above 150 do not
+// occur: the repack shift keeps them in [112, 148].  The fp32 value 2^(b-127)
+// is the byte shifted into the exponent field (b = 0 gives 0; 255 gets a
+// mantissa bit, NaN), scaled by 2^-8 exactly.
+__device__ __forceinline__ uint32_t e8m0x2_mult_f16(uint32_t two_bytes) {
+  const uint32_t b0 = two_bytes & 0xFFu, b1 = (two_bytes >> 8) & 0xFFu;
+  const float f0 = __uint_as_float((b0 << 23) | (b0 == 255u ? 0x400000u : 0u)) * 0.00390625f;
+  const float f1 = __uint_as_float((b1 << 23) | (b1 == 255u ? 0x400000u : 0u)) * 0.00390625f;
+  const __half2 h = __floats2half2_rn(f0, f1);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 // Two E4M3 bytes (low = first) -> f16x2 of value * 2^-8 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_mult_f16(uint32_t two_bytes) {

@@ -488,9 +488,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               }
             } else if (FMT == MOE_W_MXFP4) {
               const uint32_t sv = lds16(st + 2 * r);
-              const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16(sv >> 8);
-              m[j][0] = a | (a << 16);
-              m[j][1] = c | (c << 16);
+              const uint32_t ac = e8m0x2_mult_f16(sv);
+              m[j][0] = __byte_perm(ac, 0, 0x1010);
+              m[j][1] = __byte_perm(ac, 0, 0x3232);
             } else if (FMT == kFmtInt4X) {  // the row's entries of both 32-element halves
               const uint2 ev = lds64(st + 8 * r);
               m[j][0] = ev.x;

@@ -7,14 +7,15 @@
 // or relu^2 activation, or GEMM2 -- on the same packed layout, built for a
 // different bottleneck:
 //
-//   * weights reach registers, never tensor memory: eight consumer warps each
-//     own 32 rows of the 256-row tile, load their 4-bit codes from the staged
-//     chunk (one 8-byte load per row and stage, in the register-fragment order
-//     the repack writes), dequantise them in registers to fp16 and feed them
-//     as the A operand of m16n8k16 tensor-core instructions; tokens are the
-//     8-wide N side.  At 8..32 tokens a 64-K stage costs 128..512 tensor
-//     cycles per SM, under the ~380 cycles HBM needs to deliver it, and no
-//     cross-warp handoff sits between dequantisation and the MMA;
+//   * weights reach registers, never tensor memory: the consumer warps (16
+//     for 8-token blocks, 8 otherwise) each own 16 or 32 rows of the 256-row
+//     tile, load their 4-bit codes from the staged chunk (one 8-byte load per
+//     row and stage, in the register-fragment order the repack writes),
+//     dequantise them in registers to fp16 and feed them as the A operand of
+//     m16n8k16 tensor-core instructions; tokens are the 8-wide N side.  At
+//     8..32 tokens a 64-K stage costs 128..512 tensor cycles per SM, under the
+//     ~380 cycles HBM needs to deliver it, and no cross-warp handoff sits
+//     between dequantisation and the MMA;
 //   * gated GEMM1 pairs gate and up rows inside each 16-row fragment (rows
 //     0..7 gate features, rows 8..15 the same up features), so the activation
 //     is applied in the registers that hold both accumulators; non-gated GEMM1
@@ -35,9 +36,15 @@
 namespace moe {
 
 constexpr int kSmallChunk = 4;  // 64-K stages per TMA chunk
-constexpr int kSmallConsumerWarps = 8;
-constexpr int kSmallMI = kTileRows / 16 / kSmallConsumerWarps;  // 16-row fragments per consumer warp
-constexpr int kSmallThreads = (1 + kSmallConsumerWarps) * 32;
+// Consumer warps per CTA: sixteen of one 16-row fragment each for 8-token
+// blocks (the lightest per-byte work, where latency hiding needs the warps),
+// eight of two fragments otherwise.
+template <int BN>
+struct SmallCfg {
+  static constexpr int kConsumerWarps = BN == 8 ? 16 : 8;
+  static constexpr int kMI = kTileRows / 16 / kConsumerWarps;  // 16-row fragments per consumer warp
+  static constexpr int kThreads = (1 + kConsumerWarps) * 32;
+};
 
 template <int BN, int FMT>
 struct SmallSmem {
@@ -108,9 +115,9 @@ __device__ __forceinline__ void int4x8_f16_unscaled(uint32_t w, uint32_t (&o)[4]
 template <int FMT>
 __device__ __forceinline__ void fp4_row_multipliers(uint32_t sv, uint32_t (&m)[4]) {
   if (FMT == MOE_W_MXFP4) {
-    const uint32_t a = e8m0_mult_f16(sv & 0xFF), c = e8m0_mult_f16((sv >> 8) & 0xFF);
-    m[0] = a | (a << 16);
-    m[1] = c | (c << 16);
+    const uint32_t ac = e8m0x2_mult_f16(sv);
+    m[0] = __byte_perm(ac, 0, 0x1010);
+    m[1] = __byte_perm(ac, 0, 0x3232);
   } else {
     const uint32_t lo = e4m3x2_mult_f16(sv & 0xFFFF), hi = e4m3x2_mult_f16(sv >> 16);
     m[0] = __byte_perm(lo, 0, 0x1010);
@@ -121,19 +128,19 @@ __device__ __forceinline__ void fp4_row_multipliers(uint32_t sv, uint32_t (&m)[4
 }
 
 // Per-warp constants of the consumer loop (byte offsets inside a slot).
-template <int NT>
+template <int NT, int MI>
 struct SmallFrag {
   static constexpr int NQ = NT > 1 ? NT / 2 : 1;
-  int rows[kSmallMI][2];           // tile rows: row gq + 8h of 16-row fragment i
-  uint32_t code_off[kSmallMI][2];  // this lane's 8 bytes of each row inside a stage's code block
-  uint32_t sc_off[kSmallMI][2];    // each row's scale inside a scale block
+  int rows[MI][2];           // tile rows: row gq + 8h of 16-row fragment i
+  uint32_t code_off[MI][2];  // this lane's 8 bytes of each row inside a stage's code block
+  uint32_t sc_off[MI][2];    // each row's scale inside a scale block
   uint32_t b_off[4][NQ];           // ldmatrix row address of K-step j (token group q) in a stage block
 };
 
 // Activation fragments of one stage block ([BN][64] fp16, 128-byte swizzle):
 // bf[step][n-tile][0..1].
-template <int NT>
-__device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT>& F, uint32_t (&bf)[4][NT][2]) {
+template <int NT, int MI>
+__device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT, MI>& F, uint32_t (&bf)[4][NT][2]) {
   if (NT == 1) {
 #pragma unroll
     for (int j0 = 0; j0 < 4; j0 += 2)
@@ -142,7 +149,7 @@ __device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT>& F
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int q = 0; q < SmallFrag<NT>::NQ; ++q)
+      for (int q = 0; q < SmallFrag<NT, MI>::NQ; ++q)
         ldmatrix_x4(sb + F.b_off[j][q], bf[j][2 * q][0], bf[j][2 * q][1], bf[j][2 * q + 1][0], bf[j][2 * q + 1][1]);
   }
 }
@@ -151,22 +158,22 @@ __device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT>& F
 // into the accumulators.  INT4 keeps each 128-K group's sum of (q - 8) * x in
 // its own accumulators and adds it times the group's fp32 scale; FP4 scales the
 // codes in fp16 (exact).
-template <int FMT, int NT, int BN, int NST>
-__device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const SmallFrag<NT>& F,
-                                              float (&acc)[kSmallMI][NT][4], uint32_t (&m)[kSmallMI][2][4],
+template <int FMT, int NT, int BN, int NST, int MI = SmallCfg<BN>::kMI>
+__device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const SmallFrag<NT, MI>& F,
+                                              float (&acc)[MI][NT][4], uint32_t (&m)[MI][2][4],
                                               int zp_float) {
   using PF = PackedFmt<FMT>;
   if constexpr (FMT == MOE_W_INT4_U4B8) {
 #pragma unroll
     for (int gp = 0; gp < NST / 2; ++gp) {
-      float sc[kSmallMI][2];
+      float sc[MI][2];
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h) sc[i][h] = __uint_as_float(lds16(wsl + PF::stage_off(2 * gp) + F.sc_off[i][h]) << 16);
-      float part[kSmallMI][NT][4];
+      float part[MI][NT][4];
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -174,15 +181,15 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
 #pragma unroll
       for (int s2 = 0; s2 < 2; ++s2) {
         const int ss = 2 * gp + s2;
-        uint2 wv[kSmallMI][2];
+        uint2 wv[MI][2];
 #pragma unroll
-        for (int i = 0; i < kSmallMI; ++i)
+        for (int i = 0; i < MI; ++i)
 #pragma unroll
           for (int h = 0; h < 2; ++h) wv[i][h] = lds64(wsl + PF::codes_off(ss) + F.code_off[i][h]);
         uint32_t bf[4][NT][2];
-        load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
+        load_b_frags<NT, MI>(bsl + (uint32_t)(ss * BN * 128), F, bf);
 #pragma unroll
-        for (int i = 0; i < kSmallMI; ++i)
+        for (int i = 0; i < MI; ++i)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t p0[4], p1[4];  // fragment rows gq and gq + 8
@@ -196,7 +203,7 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
           }
       }
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -207,20 +214,20 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
     // codes dequantised to fp16 with it (as the tcgen05 kernel does)
 #pragma unroll
     for (int ss = 0; ss < NST; ++ss) {
-      uint2 ev[kSmallMI][2];
+      uint2 ev[MI][2];
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) ev[i][hr] = lds64(wsl + PF::stage_off(ss) + F.sc_off[i][hr]);
-      uint2 wv[kSmallMI][2];
+      uint2 wv[MI][2];
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) wv[i][hr] = lds64(wsl + PF::codes_off(ss) + F.code_off[i][hr]);
       uint32_t bf[4][NT][2];
-      load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
+      load_b_frags<NT, MI>(bsl + (uint32_t)(ss * BN * 128), F, bf);
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t p0[4], p1[4];  // fragment rows gq and gq + 8, K half h
@@ -237,21 +244,21 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
 #pragma unroll
     for (int ss = 0; ss < NST; ++ss) {
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t a = wsl + PF::stage_off(ss) + F.sc_off[i][h];
           fp4_row_multipliers<FMT>(FMT == MOE_W_MXFP4 ? lds16(a) : lds32(a), m[i][h]);
         }
-      uint2 wv[kSmallMI][2];
+      uint2 wv[MI][2];
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h) wv[i][h] = lds64(wsl + PF::codes_off(ss) + F.code_off[i][h]);
       uint32_t bf[4][NT][2];
-      load_b_frags<NT>(bsl + (uint32_t)(ss * BN * 128), F, bf);
+      load_b_frags<NT, MI>(bsl + (uint32_t)(ss * BN * 128), F, bf);
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t p0[4], p1[4];
@@ -273,13 +280,14 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
 }
 
 template <int FMT, int STAGE, int BN>
-__global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const __grid_constant__ GemmArgs g) {
+__global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1) moe_gemm_small_kernel(const __grid_constant__ GemmArgs g) {
   constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
   constexpr bool kGated = STAGE == kGemm1Gated;  // fragment rows pair gate and up features
   using SM = SmallSmem<BN, FMT>;
   constexpr int kSmallWBytes = SM::kWBytes;
   constexpr int kSlots = SM::kSlots;
   constexpr int NT = BN / 8;  // 8-token column tiles
+  constexpr int kCW = SmallCfg<BN>::kConsumerWarps, MI = SmallCfg<BN>::kMI;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
@@ -293,7 +301,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kSmallConsumerWarps);
+      mbar_init(&empty[i], kCW);
     }
     misc[1] = 0;
     mbar_init(starve, 1);
@@ -409,20 +417,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     grid_dependency_wait();
     const int cw = warp - 1;
     const int gq = lane >> 2, tq = lane & 3;
-    SmallFrag<NT> F;
-    int (&rows)[kSmallMI][2] = F.rows;
+    SmallFrag<NT, MI> F;
+    int (&rows)[MI][2] = F.rows;
 #pragma unroll
-    for (int i = 0; i < kSmallMI; ++i) {
+    for (int i = 0; i < MI; ++i) {
       if (kGated) {  // gate feature f in fragment row gq, its up row in gq + 8
-        rows[i][0] = 8 * (kSmallMI * cw + i) + gq;
+        rows[i][0] = 8 * (MI * cw + i) + gq;
         rows[i][1] = 128 + rows[i][0];
       } else {
-        rows[i][0] = 16 * (kSmallMI * cw + i) + gq;
+        rows[i][0] = 16 * (MI * cw + i) + gq;
         rows[i][1] = rows[i][0] + 8;
       }
     }
 #pragma unroll
-    for (int i = 0; i < kSmallMI; ++i)
+    for (int i = 0; i < MI; ++i)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         F.code_off[i][h] = (uint32_t)(((tq >> 1) * 256 + rows[i][h]) * 16 + (tq & 1) * 8);
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     } else {
       const uint32_t sel = (uint32_t)((lane >> 3) & 1);
 #pragma unroll
-      for (int q = 0; q < SmallFrag<NT>::NQ; ++q) {
+      for (int q = 0; q < SmallFrag<NT, MI>::NQ; ++q) {
         const uint32_t n = (uint32_t)(16 * q + (lane & 7) + 8 * (lane >> 4));
 #pragma unroll
         for (int j = 0; j < 4; ++j) F.b_off[j][q] = n * 128 + ((((uint32_t)(2 * j) + sel) ^ (n & 7)) << 4);
@@ -448,7 +456,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
     const int Npad = L.Npad;
     const int width = kGated ? 2 * Npad : (kG1 ? Npad : L.K);  // partial row width
     const int out_rows = kG1 ? Npad : L.K;                     // rows of the tile that exist
-    uint32_t m[kSmallMI][2][4] = {};
+    uint32_t m[MI][2][4] = {};
     uint32_t ck = 0;
     float vmax = 0.0f;  // largest |value| stored as fp16 (NaN ignored)
 
@@ -461,9 +469,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
         if (cw == 0 && lane == 0 && split == 0) atomicOr(g.status, kStatusRouting);
         continue;
       }
-      float acc[kSmallMI][NT][4];
+      float acc[MI][NT][4];
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i)
+      for (int i = 0; i < MI; ++i)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -489,7 +497,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       if (plan.S > 1) {
         // store this slice's fp32 partial, rows by sorted position
 #pragma unroll
-        for (int i = 0; i < kSmallMI; ++i)
+        for (int i = 0; i < MI; ++i)
 #pragma unroll
           for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -509,20 +517,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
               }
             }
         __threadfence();
-        named_bar_sync(1, kSmallConsumerWarps * 32);
+        named_bar_sync(1, kCW * 32);
         if (cw == 0 && lane == 0) {
           const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[b * plan.T + tile]),
                                          (unsigned)(plan.S - 1));
           misc[2] = old == (unsigned)(plan.S - 1) ? 1u : 0u;
         }
-        named_bar_sync(1, kSmallConsumerWarps * 32);
+        named_bar_sync(1, kCW * 32);
         const bool last = misc[2] != 0;
-        named_bar_sync(1, kSmallConsumerWarps * 32);  // misc[2] is read before the next item rewrites it
+        named_bar_sync(1, kCW * 32);  // misc[2] is read before the next item rewrites it
         if (!last) continue;
         __threadfence();
         // sum all slices in split order
 #pragma unroll
-        for (int i = 0; i < kSmallMI; ++i)
+        for (int i = 0; i < MI; ++i)
 #pragma unroll
           for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -530,7 +538,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
 #pragma unroll 4
         for (int sp = 0; sp < plan.S; ++sp)  // several slices' loads in flight at once
 #pragma unroll
-          for (int i = 0; i < kSmallMI; ++i)
+          for (int i = 0; i < MI; ++i)
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -552,7 +560,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) moe_gemm_small_kernel(const 
       }
       const float gsc = gs_tab[e];
 #pragma unroll
-      for (int i = 0; i < kSmallMI; ++i) {
+      for (int i = 0; i < MI; ++i) {
         if (kGated) {
           const int f = tile * 128 + rows[i][0];
           float bg = 0.f, bu = 0.f;
