@@ -248,14 +248,19 @@ def test_forward_smallest_shapes(fmt, K, N):
 
 
 def test_non_gated_workspace_is_smaller():
-    # relu2 banks keep N partial columns for GEMM1's split-K instead of 2N (the
-    # workspace plan reads the device's SM count, hence a GPU test)
+    # relu2 banks keep N partial columns for the tcgen05 GEMM1's split-K instead
+    # of 2N; the register-fed kernels' partial tiles ([256 rows][block_m] per
+    # CTA) do not depend on the gating, only its counters do (the plan reads the SM
+    # count, hence a GPU test)
     from weight_only_bit_moe_gb300 import binding as B
     D = B.moe_layer_desc
     for M in (1, 123, 2304):
-        g = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 0), M, 2, 16)
-        ng = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 1), M, 2, 16)
+        g = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 0), M, 2, 64)
+        ng = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 1), M, 2, 64)
         assert 0 < ng < g, (M, g, ng)
+        g16 = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 0), M, 2, 16)
+        ng16 = B.moe_workspace_size(D(0, 8, 512, 1024, 128, 0, 1, 1, 1), M, 2, 16)
+        assert 0 < ng16 <= g16, (M, g16, ng16)
 
 
 def test_device_wait_timeout_is_reported():

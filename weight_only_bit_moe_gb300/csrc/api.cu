@@ -33,6 +33,9 @@ int device_sm_count() {
   return cache[dev];
 }
 
+// Token blocks up to this size run on the register-fed kernel.
+constexpr int kSmallBlockMax = 32;
+
 // Everything the forward places in the caller's workspace, in bytes from its start.
 struct WsPlan {
   int64_t cap, blocks;
@@ -52,13 +55,24 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   w->cap = cap;
   w->blocks = cap / block_m;
   w->grid = grid;
-  // split-K only runs while tiles * blocks < grid, so the partial rows stay below this bound
-  w->rows1 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T1 + 1) * block_m);
-  w->rows2 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T2 + 1) * block_m);
-  // fp32 partial rows: GEMM1 gate and up (or h alone), GEMM2 the output width
-  const int64_t per1 = (int64_t)w->rows1 * (L.gated ? 2 : 1) * L.Npad * 4, per2 = (int64_t)w->rows2 * L.K * 4;
-  w->max_split1 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per1 ? split_budget / per1 : 1));
-  w->max_split2 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per2 ? split_budget / per2 : 1));
+  int64_t per1, per2;
+  if (block_m <= kSmallBlockMax) {
+    // register-fed kernels (stream-K, 8- and 16-token blocks): two fp32 partial tiles
+    // [256 rows][block_m] per CTA; max_split 2 turns the division on, 1 (no room, or
+    // 32-token blocks, which run whole items) falls back to whole items
+    w->rows1 = w->rows2 = 0;
+    per1 = per2 = block_m < kSmallBlockMax ? (int64_t)2 * grid * kTileRows * block_m * 4 : 0;
+    w->max_split1 = w->max_split2 = per1 > 0 && per1 <= split_budget ? 2 : 1;
+  } else {
+    // split-K only runs while tiles * blocks < grid, so the partial rows stay below this bound
+    w->rows1 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T1 + 1) * block_m);
+    w->rows2 = (int)std::min<int64_t>(cap, (int64_t)((grid - 1) / L.T2 + 1) * block_m);
+    // fp32 partial rows: GEMM1 gate and up (or h alone), GEMM2 the output width
+    per1 = (int64_t)w->rows1 * (L.gated ? 2 : 1) * L.Npad * 4;
+    per2 = (int64_t)w->rows2 * L.K * 4;
+    w->max_split1 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per1 ? split_budget / per1 : 1));
+    w->max_split2 = (int)std::max<int64_t>(1, std::min<int64_t>(kMaxSplit, per2 ? split_budget / per2 : 1));
+  }
   int64_t off = 0;
   w->status_off = off;
   off += 256;
@@ -82,10 +96,11 @@ bool plan_workspace(const Layout& L, int M, int top_k, int block_m, WsPlan* w,
   w->y_off = off;
   off = round_up64(off + pairs * L.K * 4, 256);  // y, fp32
   // (a GEMM that cannot split, max_split 1, never touches its partial area)
+  const bool streamk = block_m <= kSmallBlockMax;
   w->part1_off = off;
-  off = round_up64(off + (w->max_split1 > 1 ? (int64_t)w->max_split1 * per1 : 0), 256);
+  off = round_up64(off + (w->max_split1 > 1 ? (streamk ? 1 : (int64_t)w->max_split1) * per1 : 0), 256);
   w->part2_off = off;
-  off = round_up64(off + (w->max_split2 > 1 ? (int64_t)w->max_split2 * per2 : 0), 256);
+  off = round_up64(off + (w->max_split2 > 1 ? (streamk ? 1 : (int64_t)w->max_split2) * per2 : 0), 256);
   w->total = off;
   return true;
 }
@@ -100,8 +115,6 @@ cudaError_t launch_gemm(int fmt, bool small, int stage, int bn, const GemmArgs& 
   }
 }
 
-// Token blocks up to this size run on the register-fed kernel.
-constexpr int kSmallBlockMax = 32;
 
 bool valid_block_m(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128; }
 

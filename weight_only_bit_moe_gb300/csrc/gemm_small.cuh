@@ -24,12 +24,18 @@
 //     scales in one bulk copy, plus the block's activation rows for those
 //     stages in one 3-D TMA tile) into a 4..6-deep ring; large copies keep a
 //     single issuing thread at HBM speed;
-//   * the persistent grid, the work order (tile fastest) and the device-side
-//     split-K with last-arrival reduction in split order are those of
-//     moe_gemm_kernel; the split is chosen at period granularity.
+//   * the persistent grid walks the items (tile, token block) in the order of
+//     moe_gemm_kernel (tile fastest), but the work is divided evenly: the
+//     items' scale periods, laid end to end, are cut into one contiguous range
+//     per CTA (stream-K).  An item cut between CTAs is finished by the last of
+//     them to arrive, which sums the fp32 partials of its segments in CTA
+//     order (bitwise reproducible, no spinning).  Decode shapes rarely fill a
+//     whole number of waves, and this keeps every SM streaming to the end.
 #pragma once
 
 #include <cuda.h>
+
+#include <type_traits>
 
 #include "gemm.cuh"
 
@@ -63,35 +69,103 @@ struct SmallSmem {
   static_assert(kBBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
 };
 
-// Split-K choice in units of 1/8 stage: each wave streams ceil(units/S)
-// scale periods; a split item also writes its fp32 partial (256 rows x BN x 4 B
-// = BN/8 stages) and the last CTA of each item reads S of them back.
-__device__ __forceinline__ WorkPlan make_plan_small(const GemmArgs& g, bool gemm1, int bn) {
-  WorkPlan p;
+// Work division.  W scale periods in all (items x periods per item, item w =
+// block * T + tile); CTA c < G takes periods [c W / G, (c + 1) W / G), so
+// every CTA below G has at least one period (G <= W).  Three cases, by the
+// item count (base) against the grid:
+//   * below one wave, G = base * S: each item's K is split S ways (one segment
+//     per CTA; S weighs the shorter streams against writing and summing S
+//     partials, in 1/8-stage units);
+//   * whole items would leave over 20% of the grid's item slots idle and the
+//     items are long (>= 32 stages): G = the grid, items cut where the ranges
+//     fall (measured faster on GB300 for such shapes);
+//   * otherwise, for 32-token blocks, and whenever the workspace holds no
+//     partial area (max_split <= 1): whole items round-robin (a partly filled last wave of
+//     whole items measured faster than cut items there -- the SMs of a partial
+//     wave take a larger share of HBM).
+struct SmallPlan {
+  int nb, T, U;  // valid blocks, tiles, scale periods per item
+  int G;         // CTAs with work (stream-K)
+  int64_t W;
+  bool streamk;
+};
+
+__device__ __forceinline__ SmallPlan make_plan_small(const GemmArgs& g, bool gemm1, int bn) {
+  SmallPlan p;
   p.nb = valid_blocks(g);
   p.T = gemm1 ? g.L.T1 : g.L.T2;
-  const int stages = gemm1 ? g.L.S1 : g.L.S2;
-  p.units = stages / g.L.period;
+  p.U = (gemm1 ? g.L.S1 : g.L.S2) / g.L.period;
+  p.W = (int64_t)p.T * p.nb * p.U;
+  p.streamk = false;
+  p.G = 0;
   const int base = p.T * p.nb;
   const int grid = (int)gridDim.x;
-  int S = 1;
-  // (Only below one wave: a second, partly filled wave of whole items measured
-  // faster on GB300 than more waves of split ones -- the streaming SMs of a
-  // partial wave take a larger share of HBM.)
-  if (base > 0 && base < grid && p.nb * g.block_m <= g.split_rows) {
+  if (base <= 0 || g.max_split <= 1 || bn >= 32) return p;
+  if (base < grid) {
     const int per = g.L.period * 8;
-    int best = p.units * per;
-    const int smax = min(g.max_split, p.units);
+    int best = p.U * per + bn, S = 1;
+    const int smax = min(grid / base, p.U);
     for (int s = 2; s <= smax; ++s) {
-      const int waves = (base * s + grid - 1) / grid;
-      const int cost = waves * (((p.units + s - 1) / s) * per + bn) + s * bn;
+      const int cost = ((p.U + s - 1) / s) * per + bn + s * bn;
       if (cost < best) { best = cost; S = s; }
     }
+    if (S > 1) {
+      p.streamk = true;
+      p.G = base * S;
+      return p;
+    }
   }
-  p.S = S;
-  p.items = base * S;
+  const int waves = (base + grid - 1) / grid;
+  if (5 * base < 4 * waves * grid && p.U * g.L.period >= 32) {
+    p.streamk = true;
+    p.G = (int)(p.W < (int64_t)grid ? p.W : (int64_t)grid);
+  }
   return p;
 }
+__device__ __forceinline__ int64_t sk_lo(const SmallPlan& p, int c) { return (int64_t)c * p.W / p.G; }
+// The CTA whose range holds period u: the largest c with sk_lo(c) <= u.
+__device__ __forceinline__ int sk_owner(const SmallPlan& p, int64_t u) {
+  return (int)(((u + 1) * p.G - 1) / p.W);
+}
+
+// This CTA's segments in order: item w, periods [u0, u1) of it; `first` marks
+// the segment that opens the CTA's range (its partial slot 0; a later cut
+// segment, the range's last, uses slot 1).
+template <bool kSK>
+struct SegIter {
+  int64_t lo, u, hi;
+  int U, items, w_rr;
+  static constexpr bool streamk = kSK;
+  __device__ __forceinline__ explicit SegIter(const SmallPlan& p) {
+    U = p.U;
+    items = p.T * p.nb;
+    w_rr = blockIdx.x;
+    lo = u = hi = 0;
+    if (streamk && (int)blockIdx.x < p.G) {
+      lo = u = sk_lo(p, blockIdx.x);
+      hi = sk_lo(p, blockIdx.x + 1);
+    }
+  }
+  __device__ __forceinline__ bool next(int& w, int& u0, int& u1, bool& first) {
+    if (!streamk) {
+      if (w_rr >= items) return false;
+      w = w_rr;
+      w_rr += gridDim.x;
+      u0 = 0;
+      u1 = U;
+      first = true;
+      return true;
+    }
+    if (u >= hi) return false;
+    w = (int)(u / U);
+    const int64_t base = (int64_t)w * U;
+    u0 = (int)(u - base);
+    u1 = (int)(hi - base < (int64_t)U ? hi - base : (int64_t)U);
+    first = u == lo;
+    u = base + u1;
+    return true;
+  }
+};
 
 // 8 INT4 (uint4b8) codes of one word -> its 4 pairs of (q - 8) as f16x2, exact:
 // pairs 0 and 2 are (1024 + q) - 1032, pairs 1 and 3 (1024 + 16q) / 16 - 72.
@@ -320,316 +394,311 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1) moe_gemm_small_kern
   grid_dependents_launch();
   if (!g.align_early) grid_dependency_wait();
 
-  const WorkPlan plan = make_plan_small(g, kG1, BN);
+  const SmallPlan plan = make_plan_small(g, kG1, BN);
   const int64_t tile_bytes = kG1 ? L.tile1_bytes : L.tile2_bytes;
   const uint8_t* wbase = g.packed + (kG1 ? L.w13_off : L.w2_off);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // The whole warp runs the loop; lane 0 issues the weight copies.  GEMM1's
-    // activation rows are gathered from x (fp16, one row per token) four at a
-    // time by the warp's lanes, token = sorted id / top_k; GEMM2's are the
-    // block's rows of a (sorted order), one 3-D box per chunk.  When the
-    // alignment is older than the predecessor (align_early), the first ring's
-    // worth of weight copies go out before the wait on the predecessor and their
-    // activation copies (the predecessor's output) follow it; each slot's
-    // barrier expects both byte counts from the start.
-    const uint64_t pol = policy_evict_first();
-    int32_t* item_rows = reinterpret_cast<int32_t*>(smem + SM::kRows);
-    int32_t* pend_rows = item_rows + 32;  // [kSlots][32]
-    int pend_row[kSlots], pend_stage[kSlots], pend_nst[kSlots];
-    uint32_t npend = 0;
-    bool waited = !g.align_early;
-    uint32_t ck = 0;
-    // GEMM1 gathers token rows, unless the prologue placed them in sorted order
-    // (act-order banks, whose x columns follow each expert's order)
-    const bool gather = kG1 && !g.gemm1_rows_sorted;
-    // activation copies of chunk `stage0` (nst stages) into slot `slot`, rows from `rows`
-    auto issue_act = [&](int slot, int row0, int stage0, int nst, const int32_t* rows) {
-      const uint32_t dst = smem_u32(smem + slot * SM::kSlotBytes + kSmallWBytes);
-      if (gather) {
-        const uint32_t rows_s = smem_u32(rows);
-        for (int q = lane; q < nst * (BN / 4); q += 32) {
-          const int j = q / (BN / 4), r4 = q % (BN / 4);
-          const uint4 rv = lds128(rows_s + 16 * r4);
-          tma_gather4(dst + j * (BN * 128) + r4 * 512, &g.tmap_b, (stage0 + j) * kStageK,
-                      make_int4((int)rv.x, (int)rv.y, (int)rv.z, (int)rv.w), &full[slot]);
+  // The roles, compiled twice: with the stream-K cuts (kSK) and without them,
+  // so that whole-item launches keep the leaner code (a uniform branch picks
+  // one).  32-token blocks run whole items only: their register budget has no
+  // room for the cut path.
+  auto roles = [&](auto sk_tag) {
+    constexpr bool kSK = decltype(sk_tag)::value;
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      // The whole warp runs the loop; lane 0 issues the weight copies.  GEMM1's
+      // activation rows are gathered from x (fp16, one row per token) four at a
+      // time by the warp's lanes, token = sorted id / top_k; GEMM2's are the
+      // block's rows of a (sorted order), one 3-D box per chunk.  When the
+      // alignment is older than the predecessor (align_early), the first ring's
+      // worth of weight copies go out before the wait on the predecessor and their
+      // activation copies (the predecessor's output) follow it; each slot's
+      // barrier expects both byte counts from the start.
+      const uint64_t pol = policy_evict_first();
+      int32_t* item_rows = reinterpret_cast<int32_t*>(smem + SM::kRows);
+      int32_t* pend_rows = item_rows + 32;  // [kSlots][32]
+      int pend_row[kSlots], pend_stage[kSlots], pend_nst[kSlots];
+      uint32_t npend = 0;
+      bool waited = !g.align_early;
+      uint32_t ck = 0;
+      // GEMM1 gathers token rows, unless the prologue placed them in sorted order
+      // (act-order banks, whose x columns follow each expert's order)
+      const bool gather = kG1 && !g.gemm1_rows_sorted;
+      // activation copies of chunk `stage0` (nst stages) into slot `slot`, rows from `rows`
+      auto issue_act = [&](int slot, int row0, int stage0, int nst, const int32_t* rows) {
+        const uint32_t dst = smem_u32(smem + slot * SM::kSlotBytes + kSmallWBytes);
+        if (gather) {
+          const uint32_t rows_s = smem_u32(rows);
+          for (int q = lane; q < nst * (BN / 4); q += 32) {
+            const int j = q / (BN / 4), r4 = q % (BN / 4);
+            const uint4 rv = lds128(rows_s + 16 * r4);
+            tma_gather4(dst + j * (BN * 128) + r4 * 512, &g.tmap_b, (stage0 + j) * kStageK,
+                        make_int4((int)rv.x, (int)rv.y, (int)rv.z, (int)rv.w), &full[slot]);
+          }
+        } else if (lane == 0) {
+          tma_tile3d(dst, &g.tmap_b, 0, row0, stage0, &full[slot]);
         }
-      } else if (lane == 0) {
-        tma_tile3d(dst, &g.tmap_b, 0, row0, stage0, &full[slot]);
-      }
-    };
-    for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
-      int b, tile, split, s0, s1;
-      decode_item(plan, w, b, tile, split);
-      stage_range(plan, L, split, s0, s1);
-      const int e = block_expert(g, b);
-      if (e < 0) continue;  // (the consumers skip it too)
-      if (gather) {
-        __syncwarp();  // the previous item's rows are consumed
-        load_block_rows(g, b, BN, lane, item_rows);
-        __syncwarp();
-      }
-      const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
-      for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
-        const int c1 = min(c0 + kSmallChunk, s1);
-        const int slot = ck % kSlots;
-        if (!waited && ck == (uint32_t)kSlots) {
-          grid_dependency_wait();
-          waited = true;
-          for (uint32_t i = 0; i < npend; ++i) issue_act(i, pend_row[i], pend_stage[i], pend_nst[i], pend_rows + 32 * i);
-        }
-        mbar_wait(&empty[slot], ((ck / kSlots) + 1) & 1, abort_flag, g.status);
-        // c0 and c1 lie on scale-period boundaries
-        const int64_t off0 = (int64_t)(c0 / PackedFmt<FMT>::kPeriod) * PackedFmt<FMT>::kPeriodBytes;
-        const uint32_t wbytes = (uint32_t)((c1 - c0) / PackedFmt<FMT>::kPeriod * PackedFmt<FMT>::kPeriodBytes);
-        const uint32_t bbytes = gather ? (uint32_t)((c1 - c0) * BN * 128) : (uint32_t)SM::kBBytes;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[slot], wbytes + bbytes);
-          bulk_g2s(smem + slot * SM::kSlotBytes, tb + off0, wbytes, &full[slot], pol);
-        }
-        __syncwarp();
-        if (waited) {
-          issue_act(slot, b * g.block_m, c0, c1 - c0, item_rows);
-        } else {  // ck < kSlots: slot == ck
-          if (gather && lane < BN) pend_rows[32 * npend + lane] = item_rows[lane];
-          pend_row[npend] = b * g.block_m;
-          pend_stage[npend] = c0;
-          pend_nst[npend] = c1 - c0;
-          ++npend;
+      };
+      SegIter<kSK> seg(plan);
+      int w, u0, u1;
+      bool first;
+      while (seg.next(w, u0, u1, first)) {
+        const int tile = w % plan.T, b = w / plan.T;
+        const int s0 = u0 * L.period, s1 = u1 * L.period;
+        const int e = block_expert(g, b);
+        if (e < 0) continue;  // (the consumers skip it too)
+        if (gather) {
+          __syncwarp();  // the previous item's rows are consumed
+          load_block_rows(g, b, BN, lane, item_rows);
           __syncwarp();
         }
-      }
-    }
-    if (!waited) {
-      grid_dependency_wait();
-      for (uint32_t i = 0; i < npend; ++i) issue_act(i, pend_row[i], pend_stage[i], pend_nst[i], pend_rows + 32 * i);
-    }
-    // leave no copy in flight
-    if (lane == 0) {
-      for (uint32_t i = 0; i < (uint32_t)kSlots && i < ck; ++i) {
-        const uint32_t k = ck - 1 - i;
-        mbar_drain(&full[k % kSlots], (k / kSlots) & 1, g.status);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ consumer warps
-    grid_dependency_wait();
-    const int cw = warp - 1;
-    const int gq = lane >> 2, tq = lane & 3;
-    SmallFrag<NT, MI> F;
-    int (&rows)[MI][2] = F.rows;
-#pragma unroll
-    for (int i = 0; i < MI; ++i) {
-      if (kGated) {  // gate feature f in fragment row gq, its up row in gq + 8
-        rows[i][0] = 8 * (MI * cw + i) + gq;
-        rows[i][1] = 128 + rows[i][0];
-      } else {
-        rows[i][0] = 16 * (MI * cw + i) + gq;
-        rows[i][1] = rows[i][0] + 8;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < MI; ++i)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        F.code_off[i][h] = (uint32_t)(((tq >> 1) * 256 + rows[i][h]) * 16 + (tq & 1) * 8);
-        F.sc_off[i][h] = (uint32_t)(rows[i][h] * (FMT == kFmtInt4X ? 8 : (FMT == MOE_W_NVFP4 ? 4 : 2)));
-      }
-    // ldmatrix row addresses: token row n, 16-byte chunk c of a stage block sits
-    // at n * 128 + ((c ^ (n & 7)) << 4) (the TMA's 128-byte swizzle)
-    if (NT == 1) {
-      const uint32_t n = (uint32_t)(lane & 7), sel = (uint32_t)(lane >> 3);  // two K-steps per load
-#pragma unroll
-      for (int j = 0; j < 4; ++j) F.b_off[j][0] = n * 128 + ((((uint32_t)(2 * (j & ~1)) + sel) ^ (n & 7)) << 4);
-    } else {
-      const uint32_t sel = (uint32_t)((lane >> 3) & 1);
-#pragma unroll
-      for (int q = 0; q < SmallFrag<NT, MI>::NQ; ++q) {
-        const uint32_t n = (uint32_t)(16 * q + (lane & 7) + 8 * (lane >> 4));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) F.b_off[j][q] = n * 128 + ((((uint32_t)(2 * j) + sel) ^ (n & 7)) << 4);
-      }
-    }
-    const float* gs_tab = reinterpret_cast<const float*>(g.packed + (kG1 ? L.gs13_off : L.gs2_off));
-    const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (kG1 ? L.b13_off : L.b2_off));
-    const int Npad = L.Npad;
-    const int width = kGated ? 2 * Npad : (kG1 ? Npad : L.K);  // partial row width
-    const int out_rows = kG1 ? Npad : L.K;                     // rows of the tile that exist
-    uint32_t m[MI][2][4] = {};
-    uint32_t ck = 0;
-    float vmax = 0.0f;  // largest |value| stored as fp16 (NaN ignored)
-
-    for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
-      int b, tile, split, s0, s1;
-      decode_item(plan, w, b, tile, split);
-      stage_range(plan, L, split, s0, s1);
-      const int e = block_expert(g, b);
-      if (e < 0) {  // a block inside n_padded without one of this layer's experts
-        if (cw == 0 && lane == 0 && split == 0) atomicOr(g.status, kStatusRouting);
-        continue;
-      }
-      float acc[MI][NT][4];
-#pragma unroll
-      for (int i = 0; i < MI; ++i)
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
-
-      for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
-        const int slot = ck % kSlots;
-        mbar_wait(&full[slot], (ck / kSlots) & 1, abort_flag, g.status);
-        const uint32_t wsl = smem_u32(smem + slot * SM::kSlotBytes);
-        const uint32_t bsl = wsl + kSmallWBytes;
-        const int nst = min(kSmallChunk, s1 - c0);
-        if (nst == 4) consume_chunk<FMT, NT, BN, 4>(wsl, bsl, F, acc, m, g.zp_float);
-        else if (nst == 2) consume_chunk<FMT, NT, BN, 2>(wsl, bsl, F, acc, m, g.zp_float);
-        else if (FMT != MOE_W_INT4_U4B8) {  // INT4 chunks always hold whole 2-stage periods
-          if (nst == 3) consume_chunk<FMT, NT, BN, 3>(wsl, bsl, F, acc, m, g.zp_float);
-          else consume_chunk<FMT, NT, BN, 1>(wsl, bsl, F, acc, m, g.zp_float);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-      }
-
-      // ---------------------------------------------------------- epilogue
-      if (plan.S > 1) {
-        // store this slice's fp32 partial, rows by sorted position
-#pragma unroll
-        for (int i = 0; i < MI; ++i)
-#pragma unroll
-          for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int pos = b * g.block_m + n * 8 + 2 * tq + c;
-              float* dst = g.partial + ((int64_t)split * g.split_rows + pos) * width;
-              if (kGated) {
-                const int f = tile * 128 + rows[i][0];
-                __stcg(dst + f, acc[i][n][c]);
-                __stcg(dst + Npad + f, acc[i][n][2 + c]);
-              } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int o = tile * 256 + rows[i][h];
-                  if (o < out_rows) __stcg(dst + o, acc[i][n][2 * h + c]);
-                }
-              }
-            }
-        __threadfence();
-        named_bar_sync(1, kCW * 32);
-        if (cw == 0 && lane == 0) {
-          const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[b * plan.T + tile]),
-                                         (unsigned)(plan.S - 1));
-          misc[2] = old == (unsigned)(plan.S - 1) ? 1u : 0u;
-        }
-        named_bar_sync(1, kCW * 32);
-        const bool last = misc[2] != 0;
-        named_bar_sync(1, kCW * 32);  // misc[2] is read before the next item rewrites it
-        if (!last) continue;
-        __threadfence();
-        // sum all slices in split order
-#pragma unroll
-        for (int i = 0; i < MI; ++i)
-#pragma unroll
-          for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
-#pragma unroll 4
-        for (int sp = 0; sp < plan.S; ++sp)  // several slices' loads in flight at once
-#pragma unroll
-          for (int i = 0; i < MI; ++i)
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                const int pos = b * g.block_m + n * 8 + 2 * tq + c;
-                const float* src = g.partial + ((int64_t)sp * g.split_rows + pos) * width;
-                if (kGated) {
-                  const int f = tile * 128 + rows[i][0];
-                  acc[i][n][c] += __ldcg(src + f);
-                  acc[i][n][2 + c] += __ldcg(src + Npad + f);
-                } else {
-#pragma unroll
-                  for (int h = 0; h < 2; ++h) {
-                    const int o = tile * 256 + rows[i][h];
-                    if (o < out_rows) acc[i][n][2 * h + c] += __ldcg(src + o);
-                  }
-                }
-              }
-      }
-      const float gsc = gs_tab[e];
-#pragma unroll
-      for (int i = 0; i < MI; ++i) {
-        if (kGated) {
-          const int f = tile * 128 + rows[i][0];
-          float bg = 0.f, bu = 0.f;
-          if (g.has_bias) {
-            bg = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + f]);
-            bu = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + Npad + f]);
+        const uint8_t* tb = wbase + ((int64_t)e * plan.T + tile) * tile_bytes;
+        for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
+          const int c1 = min(c0 + kSmallChunk, s1);
+          const int slot = ck % kSlots;
+          if (!waited && ck == (uint32_t)kSlots) {
+            grid_dependency_wait();
+            waited = true;
+            for (uint32_t i = 0; i < npend; ++i) issue_act(i, pend_row[i], pend_stage[i], pend_nst[i], pend_rows + 32 * i);
           }
-#pragma unroll
+          mbar_wait(&empty[slot], ((ck / kSlots) + 1) & 1, abort_flag, g.status);
+          // c0 and c1 lie on scale-period boundaries
+          const int64_t off0 = (int64_t)(c0 / PackedFmt<FMT>::kPeriod) * PackedFmt<FMT>::kPeriodBytes;
+          const uint32_t wbytes = (uint32_t)((c1 - c0) / PackedFmt<FMT>::kPeriod * PackedFmt<FMT>::kPeriodBytes);
+          const uint32_t bbytes = gather ? (uint32_t)((c1 - c0) * BN * 128) : (uint32_t)SM::kBBytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[slot], wbytes + bbytes);
+            bulk_g2s(smem + slot * SM::kSlotBytes, tb + off0, wbytes, &full[slot], pol);
+          }
+          __syncwarp();
+          if (waited) {
+            issue_act(slot, b * g.block_m, c0, c1 - c0, item_rows);
+          } else {  // ck < kSlots: slot == ck
+            if (gather && lane < BN) pend_rows[32 * npend + lane] = item_rows[lane];
+            pend_row[npend] = b * g.block_m;
+            pend_stage[npend] = c0;
+            pend_nst[npend] = c1 - c0;
+            ++npend;
+            __syncwarp();
+          }
+        }
+      }
+      if (!waited) {
+        grid_dependency_wait();
+        for (uint32_t i = 0; i < npend; ++i) issue_act(i, pend_row[i], pend_stage[i], pend_nst[i], pend_rows + 32 * i);
+      }
+      // leave no copy in flight
+      if (lane == 0) {
+        for (uint32_t i = 0; i < (uint32_t)kSlots && i < ck; ++i) {
+          const uint32_t k = ck - 1 - i;
+          mbar_drain(&full[k % kSlots], (k / kSlots) & 1, g.status);
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ consumer warps
+      grid_dependency_wait();
+      const int cw = warp - 1;
+      const int gq = lane >> 2, tq = lane & 3;
+      SmallFrag<NT, MI> F;
+      int (&rows)[MI][2] = F.rows;
+  #pragma unroll
+      for (int i = 0; i < MI; ++i) {
+        if (kGated) {  // gate feature f in fragment row gq, its up row in gq + 8
+          rows[i][0] = 8 * (MI * cw + i) + gq;
+          rows[i][1] = 128 + rows[i][0];
+        } else {
+          rows[i][0] = 16 * (MI * cw + i) + gq;
+          rows[i][1] = rows[i][0] + 8;
+        }
+      }
+  #pragma unroll
+      for (int i = 0; i < MI; ++i)
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          F.code_off[i][h] = (uint32_t)(((tq >> 1) * 256 + rows[i][h]) * 16 + (tq & 1) * 8);
+          F.sc_off[i][h] = (uint32_t)(rows[i][h] * (FMT == kFmtInt4X ? 8 : (FMT == MOE_W_NVFP4 ? 4 : 2)));
+        }
+      // ldmatrix row addresses: token row n, 16-byte chunk c of a stage block sits
+      // at n * 128 + ((c ^ (n & 7)) << 4) (the TMA's 128-byte swizzle)
+      if (NT == 1) {
+        const uint32_t n = (uint32_t)(lane & 7), sel = (uint32_t)(lane >> 3);  // two K-steps per load
+  #pragma unroll
+        for (int j = 0; j < 4; ++j) F.b_off[j][0] = n * 128 + ((((uint32_t)(2 * (j & ~1)) + sel) ^ (n & 7)) << 4);
+      } else {
+        const uint32_t sel = (uint32_t)((lane >> 3) & 1);
+  #pragma unroll
+        for (int q = 0; q < SmallFrag<NT, MI>::NQ; ++q) {
+          const uint32_t n = (uint32_t)(16 * q + (lane & 7) + 8 * (lane >> 4));
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) F.b_off[j][q] = n * 128 + ((((uint32_t)(2 * j) + sel) ^ (n & 7)) << 4);
+        }
+      }
+      const float* gs_tab = reinterpret_cast<const float*>(g.packed + (kG1 ? L.gs13_off : L.gs2_off));
+      const uint16_t* bias_tab = reinterpret_cast<const uint16_t*>(g.packed + (kG1 ? L.b13_off : L.b2_off));
+      const int Npad = L.Npad;
+      uint32_t m[MI][2][4] = {};
+      uint32_t ck = 0;
+      float vmax = 0.0f;  // largest |value| stored as fp16 (NaN ignored)
+
+      SegIter<kSK> seg(plan);
+      int w, u0, u1;
+      bool first;
+      while (seg.next(w, u0, u1, first)) {
+        const int tile = w % plan.T, b = w / plan.T;
+        const int s0 = u0 * L.period, s1 = u1 * L.period;
+        const int e = block_expert(g, b);
+        if (e < 0) {  // a block inside n_padded without one of this layer's experts
+          if (cw == 0 && lane == 0 && u0 == 0) atomicOr(g.status, kStatusRouting);
+          continue;
+        }
+        float acc[MI][NT][4];
+  #pragma unroll
+        for (int i = 0; i < MI; ++i)
+  #pragma unroll
           for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int pos = b * g.block_m + n * 8 + 2 * tq + c;
-              const int sid = g.sorted_ids[pos];
-              if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);  // neither a pair nor padding
-              const float hg = acc[i][n][c] * gsc + bg;
-              const float hu = acc[i][n][2 + c] * gsc + bu;
-              const float a = live_sid(sid, g.pairs) ? act_fn(g.act_kind, hg, hu, g.alpha, g.limit) : 0.0f;
-              vmax = fmax_nan(vmax, fabsf(a));
-              g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
-            }
-        } else if (kG1) {  // non-gated: relu(h)^2 of each row, fp16 rows by sorted position
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int f = tile * 256 + rows[i][h];
-            const float bf = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * Npad + f]) : 0.f;
-#pragma unroll
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+
+        for (int c0 = s0; c0 < s1; c0 += kSmallChunk, ++ck) {
+          const int slot = ck % kSlots;
+          mbar_wait(&full[slot], (ck / kSlots) & 1, abort_flag, g.status);
+          const uint32_t wsl = smem_u32(smem + slot * SM::kSlotBytes);
+          const uint32_t bsl = wsl + kSmallWBytes;
+          const int nst = min(kSmallChunk, s1 - c0);
+          if (nst == 4) consume_chunk<FMT, NT, BN, 4>(wsl, bsl, F, acc, m, g.zp_float);
+          else if (nst == 2) consume_chunk<FMT, NT, BN, 2>(wsl, bsl, F, acc, m, g.zp_float);
+          else if (FMT != MOE_W_INT4_U4B8) {  // INT4 chunks always hold whole 2-stage periods
+            if (nst == 3) consume_chunk<FMT, NT, BN, 3>(wsl, bsl, F, acc, m, g.zp_float);
+            else consume_chunk<FMT, NT, BN, 1>(wsl, bsl, F, acc, m, g.zp_float);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+
+        // ---------------------------------------------------------- epilogue
+        if (kSK && (u0 > 0 || u1 < plan.U)) {
+          // a cut item: store this segment's fp32 partial ([256 tile rows][BN
+          // tokens] in the slot of this CTA's first or last segment); the last
+          // of the item's CTAs to arrive sums all of them in CTA order
+          const int slot = 2 * blockIdx.x + (first ? 0 : 1);
+          float* dst = g.partial + (int64_t)slot * kTileRows * BN;
+  #pragma unroll
+          for (int i = 0; i < MI; ++i)
+  #pragma unroll
+            for (int h = 0; h < 2; ++h)
+  #pragma unroll
+              for (int n = 0; n < NT; ++n)
+                __stcg(reinterpret_cast<float2*>(dst + rows[i][h] * BN + n * 8 + 2 * tq),
+                       make_float2(acc[i][n][2 * h], acc[i][n][2 * h + 1]));
+          __threadfence();
+          named_bar_sync(1, kCW * 32);
+          const int64_t wu = (int64_t)w * plan.U;
+          const int c_first = sk_owner(plan, wu), c_last = sk_owner(plan, wu + plan.U - 1);
+          if (cw == 0 && lane == 0) {
+            const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[w]), (unsigned)(c_last - c_first));
+            misc[2] = old == (unsigned)(c_last - c_first) ? 1u : 0u;
+          }
+          named_bar_sync(1, kCW * 32);
+          const bool last = misc[2] != 0;
+          named_bar_sync(1, kCW * 32);  // misc[2] is read before the next segment rewrites it
+          if (!last) continue;
+          __threadfence();
+  #pragma unroll
+          for (int i = 0; i < MI; ++i)
+  #pragma unroll
             for (int n = 0; n < NT; ++n)
-#pragma unroll
+  #pragma unroll
+              for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+          for (int cc = c_first; cc <= c_last; ++cc) {
+            // CTA cc holds this item in its first segment iff its range starts inside the item
+            const float* src = g.partial + (int64_t)(2 * cc + (sk_lo(plan, cc) >= wu ? 0 : 1)) * kTileRows * BN;
+  #pragma unroll
+            for (int i = 0; i < MI; ++i)
+  #pragma unroll
+              for (int h = 0; h < 2; ++h)
+  #pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                  const float2 v = __ldcg(reinterpret_cast<const float2*>(src + rows[i][h] * BN + n * 8 + 2 * tq));
+                  acc[i][n][2 * h] += v.x;
+                  acc[i][n][2 * h + 1] += v.y;
+                }
+          }
+        }
+        const float gsc = gs_tab[e];
+  #pragma unroll
+        for (int i = 0; i < MI; ++i) {
+          if (kGated) {
+            const int f = tile * 128 + rows[i][0];
+            float bg = 0.f, bu = 0.f;
+            if (g.has_bias) {
+              bg = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + f]);
+              bu = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + Npad + f]);
+            }
+  #pragma unroll
+            for (int n = 0; n < NT; ++n)
+  #pragma unroll
               for (int c = 0; c < 2; ++c) {
                 const int pos = b * g.block_m + n * 8 + 2 * tq + c;
                 const int sid = g.sorted_ids[pos];
-                if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
-                const float hv = acc[i][n][2 * h + c] * gsc + bf;
-                const bool live = live_sid(sid, g.pairs);
-                const float a = live ? relu2(hv) : 0.0f;
-                vmax = fmax_nan(vmax, fmax_nan(a, live ? hv * 0.0f : 0.0f));  // hv * 0: NaN unless finite
+                if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);  // neither a pair nor padding
+                const float hg = acc[i][n][c] * gsc + bg;
+                const float hu = acc[i][n][2 + c] * gsc + bu;
+                const float a = live_sid(sid, g.pairs) ? act_fn(g.act_kind, hg, hu, g.alpha, g.limit) : 0.0f;
+                vmax = fmax_nan(vmax, fabsf(a));
                 g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
               }
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int o = tile * 256 + rows[i][h];
-            if (o >= L.K) continue;
-            const float bo = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + o]) : 0.f;
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                const int pos = b * g.block_m + n * 8 + 2 * tq + c;
-                const int sid = g.sorted_ids[pos];
-                if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
-                if (live_sid(sid, g.pairs)) {
-                  const float y = acc[i][n][2 * h + c] * gsc + bo;
-                  vmax = fmax_nan(vmax, y * 0.0f);  // fp32 y: only a non-finite value is an error
-                  g.y_out[(int64_t)sid * L.K + o] = y;
+          } else if (kG1) {  // non-gated: relu(h)^2 of each row, fp16 rows by sorted position
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int f = tile * 256 + rows[i][h];
+              const float bf = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * Npad + f]) : 0.f;
+  #pragma unroll
+              for (int n = 0; n < NT; ++n)
+  #pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                  const int pos = b * g.block_m + n * 8 + 2 * tq + c;
+                  const int sid = g.sorted_ids[pos];
+                  if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
+                  const float hv = acc[i][n][2 * h + c] * gsc + bf;
+                  const bool live = live_sid(sid, g.pairs);
+                  const float a = live ? relu2(hv) : 0.0f;
+                  vmax = fmax_nan(vmax, fmax_nan(a, live ? hv * 0.0f : 0.0f));  // hv * 0: NaN unless finite
+                  g.a_out[(int64_t)pos * Npad + f] = __half_as_ushort(__float2half_rn(a));
                 }
-              }
+            }
+          } else {
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int o = tile * 256 + rows[i][h];
+              if (o >= L.K) continue;
+              const float bo = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + o]) : 0.f;
+  #pragma unroll
+              for (int n = 0; n < NT; ++n)
+  #pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                  const int pos = b * g.block_m + n * 8 + 2 * tq + c;
+                  const int sid = g.sorted_ids[pos];
+                  if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
+                  if (live_sid(sid, g.pairs)) {
+                    const float y = acc[i][n][2 * h + c] * gsc + bo;
+                    vmax = fmax_nan(vmax, y * 0.0f);  // fp32 y: only a non-finite value is an error
+                    g.y_out[(int64_t)sid * L.K + o] = y;
+                  }
+                }
+            }
           }
         }
       }
+      // Test hook of the failure path: after all its work, CTA 0's consumers wait
+      // on a barrier nothing arrives on.  The bounded wait gives up after the wait
+      // limit, records the timeout in the status word and the kernel ends
+      // normally, so the host reads MOE_ERR_TIMEOUT and the context stays usable.
+      if (g.test_starve_wait && blockIdx.x == 0) mbar_wait(starve, 0, abort_flag, g.status);
+      report_epilogue_status(g, vmax, cw == 0 && lane == 0, kStatusBlobFlagsSmall);
     }
-    // Test hook of the failure path: after all its work, CTA 0's consumers wait
-    // on a barrier nothing arrives on.  The bounded wait gives up after the wait
-    // limit, records the timeout in the status word and the kernel ends
-    // normally, so the host reads MOE_ERR_TIMEOUT and the context stays usable.
-    if (g.test_starve_wait && blockIdx.x == 0) mbar_wait(starve, 0, abort_flag, g.status);
-    report_epilogue_status(g, vmax, cw == 0 && lane == 0, kStatusBlobFlagsSmall);
-  }
+  };
+  if (BN < 32 && plan.streamk) roles(std::integral_constant<bool, (BN < 32)>{});
+  else roles(std::false_type{});
   __syncthreads();
 }
 
