@@ -263,10 +263,11 @@ int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void
  * workspace / workspace_bytes.  The workspace is instead a fixed array of
  * MOE_NOALLOC_SCRATCH_BYTES in this library's device image, one per device and
  * process, reserved by the CUDA runtime when the module loads; no call here
- * allocates device memory.  Its split-K partial areas are smaller than those
- * moe_w4a16_forward plans, so this entry point can pick fewer K splits;
- * results match moe_w4a16_forward's within the layer's tolerance, not bit for
- * bit.
+ * allocates device memory.  Its partial areas (split-K, and the balanced
+ * division of 8- and 16-token blocks) are smaller than those
+ * moe_w4a16_forward plans, so this entry point can split K less, or run whole
+ * items only; results match moe_w4a16_forward's within the layer's tolerance,
+ * not bit for bit.
  *   Size limit: returns MOE_ERR_WORKSPACE (nothing launched) when the shape's
  * workspace would exceed MOE_NOALLOC_SCRATCH_BYTES; moe_w4a16_forward with a
  * caller workspace handles such shapes.
@@ -283,7 +284,7 @@ int moe_w4a16_forward(const moe_layer_desc* desc, const void* packed, const void
  * operand range, inconsistent alignment inputs) are recorded in the array's
  * status word, which this entry point does not report; callers that need them
  * use moe_w4a16_forward and moe_get_status.  Decode-sized shapes may run with
- * fewer K splits (down to none) than moe_w4a16_forward would choose.
+ * fewer K splits (down to none, whole items) than moe_w4a16_forward would choose.
  *   Lifetime: the array's device address is looked up once per device and
  * cached; the library must not be used across a reset of the device
  * (cudaDeviceReset), after which the cached address is stale. */
