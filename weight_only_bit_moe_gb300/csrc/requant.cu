@@ -14,8 +14,9 @@
 // GB300 design.  The job is a pure stream (one byte in, one byte out, a
 // scale per 128), so the kernel is shaped for HBM: each warp owns one valid
 // row at a time and each lane moves 16-byte chunks (16 elements of one
-// group), every chunk's load in flight before its math, one scalar scale load
-// per chunk (the 8 lanes of a group read the same address).  The rows are
+// group), eight chunks' loads in flight before their math (4 KB per warp), one
+// scalar scale load per chunk (the 8 lanes of a group read the same address);
+// registers are capped so that three CTAs (24 row streams) share an SM.  The rows are
 // scheduled flat: each CTA scans masked_m into row offsets in shared memory
 // and maps a flat row index to (expert, row) by binary search, so a hot expert
 // spreads over the whole grid and empty experts cost nothing -- the page's two
@@ -35,7 +36,8 @@ constexpr int kRqThreads = 256;             // 8 warps, one row each at a time
 constexpr int kRqWarps = kRqThreads / 32;
 constexpr int kRqMaxExperts = 1024;
 constexpr int kRqMaxCtasPerSm = 8;          // 64 warps of row streams per SM at most
-constexpr int kRqChunksPerLane = 16;        // a row of up to 32 * 16 * 16 = 8192 elements in one pass
+constexpr int kRqResident = 3;              // CTAs that fit on an SM at once (registers capped for it)
+constexpr int kRqChunksPerLane = 8;         // 4 KB of a row in flight per warp per pass
 
 struct RequantArgs {
   const uint8_t* x;
@@ -70,7 +72,7 @@ __device__ __forceinline__ uint4 requant16(uint4 v, float s, float r) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(kRqThreads) requant_kernel(const __grid_constant__ RequantArgs a) {
+__global__ void __launch_bounds__(kRqThreads, kRqResident) requant_kernel(const __grid_constant__ RequantArgs a) {
   __shared__ int row_start[kRqMaxExperts + 1];  // flat index of each expert's first valid row
   __shared__ int warp_tot[kRqWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
