@@ -147,7 +147,7 @@ def test_block_m_chooser(lib):
     assert lib.moe_choose_block_m(d, 1024, 8, 128) == 128    # int4, 64 rows: vs 64
     assert lib.moe_choose_block_m(d, 4096, 8, 128) == 128    # vs 64
     assert lib.moe_choose_block_m(nv, 128, 8, 256) == 8      # nvfp4, 4 rows: vs 64
-    assert lib.moe_choose_block_m(nv, 256, 8, 256) == 16     # nvfp4, 8 rows: vs 8 and 64
+    assert lib.moe_choose_block_m(nv, 256, 8, 256) == 64     # nvfp4, 8 rows: vs 8 and 16
     assert lib.moe_choose_block_m(nv, 512, 8, 256) == 64     # nvfp4, 16 rows: vs 16 and 32
     assert lib.moe_choose_block_m(mx, 32, 4, 32) == 8        # mxfp4, 4 rows: vs 16
     assert lib.moe_choose_block_m(mx, 64, 4, 32) == 64       # mxfp4, 8 rows: vs 8 and 16

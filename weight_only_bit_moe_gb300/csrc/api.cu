@@ -200,14 +200,14 @@ extern "C" int moe_choose_block_m(const moe_layer_desc* desc, int M, int top_k, 
   //                      8     16    32 (register-fed)   64    128 (tcgen05)
   //   INT4              0.86  1     1.56                1.32  1.68
   //   MXFP4             0.86  1     1.34                0.93  1.09
-  //   NVFP4             0.86  1     1.34                1.08  1.26
+  //   NVFP4             0.86  1     1.34                0.94  1.26
   // Below K = 1024 the tcgen05 tiles are too short for those costs: the
   // register-fed sizes serve up to 32 rows and 64-token tiles the rest (with
   // 128-token tiles the epilogue, which does not overlap the next tile's MMAs
   // there, outweighs the better MMA rate).
   const bool int4 = desc->fmt == MOE_W_INT4_U4B8, mx = desc->fmt == MOE_W_MXFP4;
   const int sizes[5] = {8, 16, 32, 64, 128};
-  const double cost[5] = {0.86, 1.0, int4 ? 1.56 : 1.34, int4 ? 1.32 : (mx ? 0.93 : 1.08),
+  const double cost[5] = {0.86, 1.0, int4 ? 1.56 : 1.34, int4 ? 1.32 : (mx ? 0.93 : 0.94),
                           int4 ? 1.68 : (mx ? 1.09 : 1.26)};
   const bool short_k = desc->hidden < 1024;
   if (short_k && rows > 32.0) return 64;
