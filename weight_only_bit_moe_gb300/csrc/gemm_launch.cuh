@@ -58,7 +58,7 @@ cudaError_t launch_gemm_small_instance(const GemmArgs& g, int grid, cudaStream_t
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
-  return launch_dependent(moe_gemm_small_kernel<FMT, STAGE, BN>, dim3(grid), dim3(SmallCfg<BN>::kThreads),
+  return launch_dependent(moe_gemm_small_kernel<FMT, STAGE, BN>, dim3(grid), dim3(SmallCfg<BN, STAGE>::kThreads),
                           SmallSmem<BN, FMT>::kAlloc, st, g);
 }
 

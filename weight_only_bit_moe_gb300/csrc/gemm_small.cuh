@@ -43,11 +43,12 @@ namespace moe {
 
 constexpr int kSmallChunk = 4;  // 64-K stages per TMA chunk
 // Consumer warps per CTA: sixteen of one 16-row fragment each for 8-token
-// blocks (the lightest per-byte work, where latency hiding needs the warps),
-// eight of two fragments otherwise.
-template <int BN>
+// blocks and for GEMM2's 16-token blocks (the lightest per-byte work, where
+// latency hiding needs the warps), eight of two fragments otherwise (16-token
+// GEMM1 measured slower with sixteen: its gated fragments keep more state).
+template <int BN, int STAGE>
 struct SmallCfg {
-  static constexpr int kConsumerWarps = BN == 8 ? 16 : 8;
+  static constexpr int kConsumerWarps = (BN == 8 || (BN == 16 && STAGE == kGemm2)) ? 16 : 8;
   static constexpr int kMI = kTileRows / 16 / kConsumerWarps;  // 16-row fragments per consumer warp
   static constexpr int kThreads = (1 + kConsumerWarps) * 32;
 };
@@ -232,7 +233,7 @@ __device__ __forceinline__ void load_b_frags(uint32_t sb, const SmallFrag<NT, MI
 // into the accumulators.  INT4 keeps each 128-K group's sum of (q - 8) * x in
 // its own accumulators and adds it times the group's fp32 scale; FP4 scales the
 // codes in fp16 (exact).
-template <int FMT, int NT, int BN, int NST, int MI = SmallCfg<BN>::kMI>
+template <int FMT, int NT, int BN, int NST, int MI>
 __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const SmallFrag<NT, MI>& F,
                                               float (&acc)[MI][NT][4], uint32_t (&m)[MI][2][4],
                                               int zp_float) {
@@ -354,14 +355,14 @@ __device__ __forceinline__ void consume_chunk(uint32_t wsl, uint32_t bsl, const 
 }
 
 template <int FMT, int STAGE, int BN>
-__global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1) moe_gemm_small_kernel(const __grid_constant__ GemmArgs g) {
+__global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_small_kernel(const __grid_constant__ GemmArgs g) {
   constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
   constexpr bool kGated = STAGE == kGemm1Gated;  // fragment rows pair gate and up features
   using SM = SmallSmem<BN, FMT>;
   constexpr int kSmallWBytes = SM::kWBytes;
   constexpr int kSlots = SM::kSlots;
   constexpr int NT = BN / 8;  // 8-token column tiles
-  constexpr int kCW = SmallCfg<BN>::kConsumerWarps, MI = SmallCfg<BN>::kMI;
+  constexpr int kCW = SmallCfg<BN, STAGE>::kConsumerWarps, MI = SmallCfg<BN, STAGE>::kMI;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBar);
@@ -565,11 +566,11 @@ __global__ void __launch_bounds__(SmallCfg<BN>::kThreads, 1) moe_gemm_small_kern
           const uint32_t wsl = smem_u32(smem + slot * SM::kSlotBytes);
           const uint32_t bsl = wsl + kSmallWBytes;
           const int nst = min(kSmallChunk, s1 - c0);
-          if (nst == 4) consume_chunk<FMT, NT, BN, 4>(wsl, bsl, F, acc, m, g.zp_float);
-          else if (nst == 2) consume_chunk<FMT, NT, BN, 2>(wsl, bsl, F, acc, m, g.zp_float);
+          if (nst == 4) consume_chunk<FMT, NT, BN, 4, MI>(wsl, bsl, F, acc, m, g.zp_float);
+          else if (nst == 2) consume_chunk<FMT, NT, BN, 2, MI>(wsl, bsl, F, acc, m, g.zp_float);
           else if (FMT != MOE_W_INT4_U4B8) {  // INT4 chunks always hold whole 2-stage periods
-            if (nst == 3) consume_chunk<FMT, NT, BN, 3>(wsl, bsl, F, acc, m, g.zp_float);
-            else consume_chunk<FMT, NT, BN, 1>(wsl, bsl, F, acc, m, g.zp_float);
+            if (nst == 3) consume_chunk<FMT, NT, BN, 3, MI>(wsl, bsl, F, acc, m, g.zp_float);
+            else consume_chunk<FMT, NT, BN, 1, MI>(wsl, bsl, F, acc, m, g.zp_float);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot]);
