@@ -48,7 +48,7 @@ constexpr int kSmallChunk = 4;  // 64-K stages per TMA chunk
 // GEMM1 measured slower with sixteen: its gated fragments keep more state).
 template <int BN, int STAGE>
 struct SmallCfg {
-  static constexpr int kConsumerWarps = (BN == 8 || (BN == 16 && STAGE == kGemm2)) ? 16 : 8;
+  static constexpr int kConsumerWarps = (BN == 8 || (BN <= 32 && STAGE == kGemm2)) ? 16 : 8;
   static constexpr int kMI = kTileRows / 16 / kConsumerWarps;  // 16-row fragments per consumer warp
   static constexpr int kThreads = (1 + kConsumerWarps) * 32;
 };
