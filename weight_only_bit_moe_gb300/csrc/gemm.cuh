@@ -355,7 +355,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer (packed weights)
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      // every token block of an expert streams the same tiles: keep them for the
+      // blocks that follow (the tile-fastest order runs them close together)
+      const uint64_t pol = policy_evict_normal();
       uint32_t pk = 0;
       for (int w = blockIdx.x; w < plan.items; w += gridDim.x) {
         int b, tile, split, s0, s1;
