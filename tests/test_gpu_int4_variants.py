@@ -90,14 +90,27 @@ def test_act_order_groups_must_be_whole():
     assert layer.status() == B.MOE_ERR_UNSUPPORTED
 
 
-def test_int4_variant_full_shape():
-    # zero points and act-order at the K=4096, N=1536, E=128, top_k=8 shape (M=256),
-    # every token against the oracle
-    wl = dataclasses.replace(wk.WORKLOADS["int4-uniform"], act_order=True, zero_kind="int", group_size=64)
-    W = wk.make_weights(wl, 231)
-    X = wk.make_batch(wl, 256, 232)
-    from weight_only_bit_moe_gb300.layer import MoELayer
-    layer = MoELayer.from_numpy(W)
+_full_variant = {}
+
+
+def _full_variant_layer():
+    if not _full_variant:
+        from weight_only_bit_moe_gb300.layer import MoELayer
+        wl = dataclasses.replace(wk.WORKLOADS["int4-uniform"], act_order=True, zero_kind="int", group_size=64)
+        W = wk.make_weights(wl, 231)
+        _full_variant["v"] = (wl, W, MoELayer.from_numpy(W))
+    return _full_variant["v"]
+
+
+@pytest.mark.parametrize("M", [1, 2, 256])
+def test_int4_variant_full_shape(M):
+    # zero points and act-order at the K=4096, N=1536, E=128, top_k=8 shape, every
+    # token against the oracle: M=1 and 2 run the register-fed kernels with their
+    # K cut across CTAs (stream-K), M=256 the tcgen05 kernels
+    from weight_only_bit_moe_gb300 import binding as B
+    wl, W, layer = _full_variant_layer()
+    X = wk.make_batch(wl, M, 232 + M)
     out = run_layer(layer, wl, X)
+    assert layer.status() == B.MOE_OK
     ref = bf16_to_f32(oracle.forward_workload(wl, W, X))
-    check_workload(out.float().cpu().numpy(), ref, wl, "int4 zp act-order M=256")
+    check_workload(out.float().cpu().numpy(), ref, wl, f"int4 zp act-order M={M}")
