@@ -627,16 +627,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[accb]);
-        __threadfence();
+        // the CTA barrier orders every epilogue thread's partial stores before one
+        // thread's fence and arrival (release); the last CTA's arriving thread fences
+        // again before the barrier that lets the others read the partials (acquire)
         named_bar_sync(1, kEpiThreads);
         if (et == 0) {
+          __threadfence();
           const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[b * plan.T + tile]),
                                          (unsigned)(plan.S - 1));
           misc[2] = old == (unsigned)(plan.S - 1) ? 1u : 0u;
+          __threadfence();
         }
         named_bar_sync(1, kEpiThreads);
         finish = misc[2] != 0;
-        if (finish) __threadfence();
       }
       if (finish) {
         // This thread's token columns come in batches of 8: c0 = 8 * csub + 16 * it.

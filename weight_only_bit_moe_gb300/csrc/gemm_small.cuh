@@ -591,19 +591,22 @@ __global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_sma
               for (int n = 0; n < NT; ++n)
                 __stcg(reinterpret_cast<float2*>(dst + rows[i][h] * BN + n * 8 + 2 * tq),
                        make_float2(acc[i][n][2 * h], acc[i][n][2 * h + 1]));
-          __threadfence();
+          // the CTA barrier orders every consumer's partial stores before one thread's
+          // fence and arrival (release); the last CTA's arriving thread fences again
+          // before the barrier that lets its warps read the others' partials (acquire)
           named_bar_sync(1, kCW * 32);
           const int64_t wu = (int64_t)w * plan.U;
           const int c_first = sk_owner(plan, wu), c_last = sk_owner(plan, wu + plan.U - 1);
           if (cw == 0 && lane == 0) {
+            __threadfence();
             const unsigned old = atomicInc(reinterpret_cast<unsigned*>(&g.counters[w]), (unsigned)(c_last - c_first));
             misc[2] = old == (unsigned)(c_last - c_first) ? 1u : 0u;
+            __threadfence();
           }
           named_bar_sync(1, kCW * 32);
           const bool last = misc[2] != 0;
           named_bar_sync(1, kCW * 32);  // misc[2] is read before the next segment rewrites it
           if (!last) continue;
-          __threadfence();
   #pragma unroll
           for (int i = 0; i < MI; ++i)
   #pragma unroll
