@@ -33,7 +33,8 @@
 //     reproducible, no spinning);
 //   * one elected lane of the MMA warp issues tcgen05.mma into TMEM accumulators (double-buffered up
 //     to 64 tokens); eight epilogue warps (two per TMEM lane quarter, splitting
-//     the token columns) add bias and scales, apply the activation (GEMM1:
+//     the token columns; sixteen for MXFP4 at 128-token tiles, GemmCfg) add
+//     bias and scales, apply the activation (GEMM1:
 //     act(gate, up) of a lane's two halves, or relu(h)^2 of each half for
 //     non-gated experts) or write rows to their pairs (GEMM2).
 #pragma once
@@ -46,11 +47,19 @@ namespace moe {
 
 constexpr int kSup = 2;                // 64-K stages per pipeline unit (one barrier round per unit)
 constexpr int kNumDequantWarps = 8;
-constexpr int kNumEpiWarps = 8;                             // two per TMEM lane quarter
-constexpr int kEpiThreads = kNumEpiWarps * 32;
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpBProducer = 2, kWarpDequant0 = 3;
 constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..18
-constexpr int kGemmThreads = (kWarpEpi0 + kNumEpiWarps) * 32;  // 608
+// Epilogue warps: eight (two per TMEM lane quarter), or sixteen for MXFP4 at
+// 128-token tiles, whose epilogue then drains the accumulator in half the time
+// (GEMM1 and GEMM2 7-9 % faster at mxfp4 M=1024; with sixteen the kernel fits
+// 72 registers a thread, which slowed the INT4 dequant and the 64-token tiles).
+template <int FMT, int BN>
+struct GemmCfg {
+  static constexpr int kEpiWarps = (FMT == MOE_W_MXFP4 && BN == 128) ? 16 : 8;
+  static constexpr int kEpiThreads = kEpiWarps * 32;
+  static constexpr int kEpiColStep = 8 * (kEpiWarps / 4);  // a warp's 8-column batches lie this far apart
+  static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;  // 608 or 864
+};
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint32_t kTmemCols = 512;                         // whole TMEM (one CTA per SM)
 constexpr uint32_t kAColsPerStage = 64;                     // 2 halves x 64 K / 2 per column
@@ -290,13 +299,15 @@ __device__ __forceinline__ void load_block_rows(const GemmArgs& g, int b, int n,
 }
 
 template <int FMT, int STAGE, int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
+__global__ void __launch_bounds__(GemmCfg<FMT, BN>::kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
   constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
   constexpr bool kGated = STAGE == kGemm1Gated;  // tile halves are gate and up rows
   using SM = GemmSmem<BN, FMT>;
   constexpr int kPackedSlotBytes = SM::kPackedSlotBytes;
   using PF = PackedFmt<FMT>;
   constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc, kSA = SM::kSA;
+  constexpr int kNumEpiWarps = GemmCfg<FMT, BN>::kEpiWarps, kEpiThreads = GemmCfg<FMT, BN>::kEpiThreads;
+  constexpr int kEpiColStep = GemmCfg<FMT, BN>::kEpiColStep;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBar);
@@ -611,7 +622,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       bool finish = true;  // this CTA writes final results for the item
       if (plan.S > 1) {
         // split-K: store the fp32 partial of this slice, rows by sorted position
-        for (int c0 = 8 * csub; c0 < BN; c0 += 16) {
+        for (int c0 = 8 * csub; c0 < BN; c0 += kEpiColStep) {
           uint32_t v0[8], v1[8];
           tmem_ld8(tb + c0, v0);
           tmem_ld8(tb + BN + c0, v1);
@@ -642,11 +653,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         finish = misc[2] != 0;
       }
       if (finish) {
-        // This thread's token columns come in batches of 8: c0 = 8 * csub + 16 * it.
+        // This thread's token columns come in batches of 8: c0 = 8 * csub + kEpiColStep * it.
         // Each batch loads its 8 sorted ids at once, computes all 8 values and then
         // stores them, so the columns overlap; the next batch's accumulators are
         // requested from TMEM before this batch's math.
-        constexpr int kIters = BN / 16;
+        constexpr int kIters = BN / kEpiColStep;
         uint32_t v0[8], v1[8];
         if (plan.S == 1) {
           tmem_ld8(tb + 8 * csub, v0);
@@ -654,15 +665,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         }
 #pragma unroll 1
         for (int it = 0; it < kIters; ++it) {
-          const int c0 = 8 * csub + 16 * it;
+          const int c0 = 8 * csub + kEpiColStep * it;
           float f0[8], f1[8];
           if (plan.S == 1) {
             tmem_ld_wait();
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) { f0[jj] = __uint_as_float(v0[jj]); f1[jj] = __uint_as_float(v1[jj]); }
             if (it + 1 < kIters) {
-              tmem_ld8(tb + c0 + 16, v0);
-              tmem_ld8(tb + BN + c0 + 16, v1);
+              tmem_ld8(tb + c0 + kEpiColStep, v0);
+              tmem_ld8(tb + BN + c0 + kEpiColStep, v1);
             } else {  // every accumulator column of this thread is in registers
               tc_fence_before();
               __syncwarp();
