@@ -33,7 +33,7 @@
 //     reproducible, no spinning);
 //   * one elected lane of the MMA warp issues tcgen05.mma into TMEM accumulators (double-buffered up
 //     to 64 tokens); eight epilogue warps (two per TMEM lane quarter, splitting
-//     the token columns; sixteen for MXFP4 at 128-token tiles, GemmCfg) add
+//     the token columns; sixteen in some 128-token instances, GemmCfg) add
 //     bias and scales, apply the activation (GEMM1:
 //     act(gate, up) of a lane's two halves, or relu(h)^2 of each half for
 //     non-gated experts) or write rows to their pairs (GEMM2).
@@ -49,13 +49,14 @@ constexpr int kSup = 2;                // 64-K stages per pipeline unit (one bar
 constexpr int kNumDequantWarps = 8;
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpBProducer = 2, kWarpDequant0 = 3;
 constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..18
-// Epilogue warps: eight (two per TMEM lane quarter), or sixteen for MXFP4 at
-// 128-token tiles, whose epilogue then drains the accumulator in half the time
-// (GEMM1 and GEMM2 7-9 % faster at mxfp4 M=1024; with sixteen the kernel fits
-// 72 registers a thread, which slowed the INT4 dequant and the 64-token tiles).
-template <int FMT, int BN>
+// Epilogue warps: eight (two per TMEM lane quarter), or sixteen at 128-token
+// tiles for the FP4 formats and for GEMM2, whose epilogue then drains the
+// accumulator in half the time (mxfp4 M=1024 and nvfp4 M=1024..2048 5-8 %
+// faster); with sixteen the kernel fits 72 registers a thread, which slowed the
+// INT4 GEMM1 dequant and the 64-token tiles.
+template <int FMT, int BN, int STAGE>
 struct GemmCfg {
-  static constexpr int kEpiWarps = (FMT == MOE_W_MXFP4 && BN == 128) ? 16 : 8;
+  static constexpr int kEpiWarps = (BN == 128 && (FMT == MOE_W_MXFP4 || FMT == MOE_W_NVFP4 || STAGE == kGemm2)) ? 16 : 8;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kEpiColStep = 8 * (kEpiWarps / 4);  // a warp's 8-column batches lie this far apart
   static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;  // 608 or 864
@@ -299,15 +300,15 @@ __device__ __forceinline__ void load_block_rows(const GemmArgs& g, int b, int n,
 }
 
 template <int FMT, int STAGE, int BN>
-__global__ void __launch_bounds__(GemmCfg<FMT, BN>::kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
+__global__ void __launch_bounds__(GemmCfg<FMT, BN, STAGE>::kThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmArgs g) {
   constexpr bool kG1 = STAGE != kGemm2;          // reads w13 (x rows) rather than w2 (a rows)
   constexpr bool kGated = STAGE == kGemm1Gated;  // tile halves are gate and up rows
   using SM = GemmSmem<BN, FMT>;
   constexpr int kPackedSlotBytes = SM::kPackedSlotBytes;
   using PF = PackedFmt<FMT>;
   constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc, kSA = SM::kSA;
-  constexpr int kNumEpiWarps = GemmCfg<FMT, BN>::kEpiWarps, kEpiThreads = GemmCfg<FMT, BN>::kEpiThreads;
-  constexpr int kEpiColStep = GemmCfg<FMT, BN>::kEpiColStep;
+  constexpr int kNumEpiWarps = GemmCfg<FMT, BN, STAGE>::kEpiWarps, kEpiThreads = GemmCfg<FMT, BN, STAGE>::kEpiThreads;
+  constexpr int kEpiColStep = GemmCfg<FMT, BN, STAGE>::kEpiColStep;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBar);

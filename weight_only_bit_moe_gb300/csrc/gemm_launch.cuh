@@ -22,7 +22,7 @@ cudaError_t launch_gemm_instance(const GemmArgs& g, int grid, cudaStream_t st) {
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
-  return launch_dependent(moe_gemm_kernel<FMT, STAGE, BN>, dim3(grid), dim3(GemmCfg<FMT, BN>::kThreads), GemmSmem<BN, FMT>::kAlloc, st, g);
+  return launch_dependent(moe_gemm_kernel<FMT, STAGE, BN>, dim3(grid), dim3(GemmCfg<FMT, BN, STAGE>::kThreads), GemmSmem<BN, FMT>::kAlloc, st, g);
 }
 
 template <int FMT, int BN>
