@@ -56,7 +56,7 @@ constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..18
 // INT4 GEMM1 dequant and the 64-token tiles.
 template <int FMT, int BN, int STAGE>
 struct GemmCfg {
-  static constexpr int kEpiWarps = (BN == 128 && (FMT == MOE_W_MXFP4 || FMT == MOE_W_NVFP4 || STAGE == kGemm2)) ? 16 : 8;
+  static constexpr int kEpiWarps = BN == 128 ? 16 : 8;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kEpiColStep = 8 * (kEpiWarps / 4);  // a warp's 8-column batches lie this far apart
   static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;  // 608 or 864
@@ -524,46 +524,47 @@ __global__ void __launch_bounds__(GemmCfg<FMT, BN, STAGE>::kThreads, 1) moe_gemm
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_empty[ps]);
-        // the first stage is dequantised before the wait for its TMEM slot, so
-        // only the stores trail the MMAs that free it
+        // the first half of the first stage is dequantised before the wait for its
+        // TMEM slot, so mostly the stores trail the MMAs that free it
 #pragma unroll
         for (int j = 0; j < kSup; ++j) {
           if (j < nst) {
             const uint32_t wd[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
                                     u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
-            uint32_t o[32];  // TMEM column c = K pair (2c, 2c+1) of the stage
-            if (FMT == kFmtInt4X) {
-              // words of one 32-element half share its entry: h outer
+            // each 32-element half of the stage (TMEM columns 16h .. 16h+15, column c =
+            // K pair (2c, 2c+1)) is dequantised into 16 registers and stored on its own
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 2; ++h) {
+              uint32_t o[16];
+              if (FMT == kFmtInt4X) {  // the words of a half share its entry
                 const Int4ZpConst kc = int4zp_const(m[j][h], g.zp_float);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                   uint32_t t4[4];
                   int4x8_f16_zp(wd[2 * t + h], kc, t4);
 #pragma unroll
-                  for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
+                  for (int p = 0; p < 4; ++p) o[t + 4 * p] = t4[p];
+                }
+              } else {
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
+                  // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
+                  const int v = 2 * t + h;
+                  uint32_t t4[4];
+                  if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[j][0], m[j][1], t4);
+                  else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[j][h], m[j][h], t4);
+                  else e2m1x8_f16(wd[v], m[j][2 * h], m[j][2 * h + 1], t4);
+#pragma unroll
+                  for (int p = 0; p < 4; ++p) o[t + 4 * p] = t4[p];
                 }
               }
-            } else {
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
-                // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
-                const int t = v >> 1, h = v & 1;
-                uint32_t t4[4];
-                if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[j][0], m[j][1], t4);
-                else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[j][h], m[j][h], t4);
-                else e2m1x8_f16(wd[v], m[j][2 * h], m[j][2 * h + 1], t4);
-#pragma unroll
-                for (int p = 0; p < 4; ++p) o[16 * h + t + 4 * p] = t4[p];
+              if (j == 0 && h == 0) {
+                mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
+                tc_fence_after();
               }
+              tmem_st16(t_lane + as * kAColsPerUnit + j * kAColsPerStage + 16 * h, o);
             }
-            if (j == 0) {
-              mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
-              tc_fence_after();
-            }
-            tmem_st32(t_lane + as * kAColsPerUnit + j * kAColsPerStage, o);
           }
         }
         tmem_st_wait();
