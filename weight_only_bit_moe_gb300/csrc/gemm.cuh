@@ -49,14 +49,14 @@ constexpr int kSup = 2;                // 64-K stages per pipeline unit (one bar
 constexpr int kNumDequantWarps = 8;
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpBProducer = 2, kWarpDequant0 = 3;
 constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..18
-// Epilogue warps: eight (two per TMEM lane quarter), or sixteen at 128-token
-// tiles for the FP4 formats and for GEMM2, whose epilogue then drains the
-// accumulator in half the time (mxfp4 M=1024 and nvfp4 M=1024..2048 5-8 %
-// faster); with sixteen the kernel fits 72 registers a thread, which slowed the
-// INT4 GEMM1 dequant and the 64-token tiles.
+// Epilogue warps: sixteen (four per TMEM lane quarter) at 128-token tiles and
+// for the FP4 formats, whose epilogues then drain the accumulator in half the
+// time (headline GEMM2 453 -> 422 us, mxfp4 M=1024 275 -> 248 us, nvfp4 M=512
+// -2.5 %); eight for INT4 at 64-token tiles, which measured 1-3 % slower with
+// sixteen in the 72 registers a thread that an 864-thread CTA leaves.
 template <int FMT, int BN, int STAGE>
 struct GemmCfg {
-  static constexpr int kEpiWarps = BN == 128 ? 16 : 8;
+  static constexpr int kEpiWarps = (BN == 128 || FMT == MOE_W_MXFP4 || FMT == MOE_W_NVFP4) ? 16 : 8;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kEpiColStep = 8 * (kEpiWarps / 4);  // a warp's 8-column batches lie this far apart
   static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;  // 608 or 864
