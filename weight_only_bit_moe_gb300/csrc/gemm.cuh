@@ -46,17 +46,25 @@
 namespace moe {
 
 constexpr int kSup = 2;                // 64-K stages per pipeline unit (one barrier round per unit)
-constexpr int kNumDequantWarps = 8;
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpBProducer = 2, kWarpDequant0 = 3;
-constexpr int kWarpEpi0 = kWarpDequant0 + kNumDequantWarps;  // 11..18
-// Epilogue warps: sixteen (four per TMEM lane quarter) at 128-token tiles and
-// for the FP4 formats, whose epilogues then drain the accumulator in half the
-// time (headline GEMM2 453 -> 422 us, mxfp4 M=1024 275 -> 248 us, nvfp4 M=512
-// -2.5 %); eight for INT4 at 64-token tiles, which measured 1-3 % slower with
-// sixteen in the 72 registers a thread that an 864-thread CTA leaves.
+// Warp roles per instance.  Dequant warps: eight, one per TMEM lane quarter
+// and 128-row half, each thread one row of a whole 64-element stage.  The
+// kernel also supports sixteen, the two 32-element halves of a stage on two
+// warps (kSplitDq); within the 864 threads a CTA can run at 72 registers that
+// leaves eight epilogue warps, and INT4 GEMM1 at 128-token tiles measured
+// slower that way (headline GEMM1 725 -> 773 us), so every instance runs
+// eight.  Epilogue warps: sixteen (four per TMEM lane quarter) at 128-token
+// tiles and for the FP4 formats, whose epilogues then drain the accumulator in
+// half the time (headline GEMM2 453 -> 422 us, mxfp4 M=1024 275 -> 248 us,
+// nvfp4 M=512 -2.5 %); eight for INT4 at 64-token tiles, which measured 1-3 %
+// slower with sixteen in the 72 registers a thread that an 864-thread CTA
+// leaves.
 template <int FMT, int BN, int STAGE>
 struct GemmCfg {
-  static constexpr int kEpiWarps = (BN == 128 || FMT == MOE_W_MXFP4 || FMT == MOE_W_NVFP4) ? 16 : 8;
+  static constexpr bool kSplitDq = false;
+  static constexpr int kDqWarps = kSplitDq ? 16 : 8;
+  static constexpr int kEpiWarps = kSplitDq ? 8 : ((BN == 128 || FMT == MOE_W_MXFP4 || FMT == MOE_W_NVFP4) ? 16 : 8);
+  static constexpr int kWarpEpi0 = kWarpDequant0 + kDqWarps;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kEpiColStep = 8 * (kEpiWarps / 4);  // a warp's 8-column batches lie this far apart
   static constexpr int kThreads = (kWarpEpi0 + kEpiWarps) * 32;  // 608 or 864
@@ -307,8 +315,9 @@ __global__ void __launch_bounds__(GemmCfg<FMT, BN, STAGE>::kThreads, 1) moe_gemm
   constexpr int kPackedSlotBytes = SM::kPackedSlotBytes;
   using PF = PackedFmt<FMT>;
   constexpr int kSB = SM::kSB, kSP = SM::kSP, kNacc = SM::kNacc, kSA = SM::kSA;
-  constexpr int kNumEpiWarps = GemmCfg<FMT, BN, STAGE>::kEpiWarps, kEpiThreads = GemmCfg<FMT, BN, STAGE>::kEpiThreads;
-  constexpr int kEpiColStep = GemmCfg<FMT, BN, STAGE>::kEpiColStep;
+  using Cfg = GemmCfg<FMT, BN, STAGE>;
+  constexpr int kNumEpiWarps = Cfg::kEpiWarps, kEpiThreads = Cfg::kEpiThreads, kEpiColStep = Cfg::kEpiColStep;
+  constexpr int kNumDequantWarps = Cfg::kDqWarps, kWarpEpi0 = Cfg::kWarpEpi0;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBar);
@@ -468,7 +477,9 @@ __global__ void __launch_bounds__(GemmCfg<FMT, BN, STAGE>::kThreads, 1) moe_gemm
     // ------------------------------------------------------------ dequant warps
     // warp -> (TMEM lane quarter q = warp % 4, half): a warp may only touch TMEM
     // lanes 32q..32q+31; each thread dequantises one tile row per stage
-    const int q = warp & 3, half = (warp - kWarpDequant0) >> 2;
+    // (with sixteen warps, kh = which 32-element half of every stage the warp takes)
+    const int q = warp & 3, half = ((warp - kWarpDequant0) >> 2) & 1, kh = (warp - kWarpDequant0) >> 3;
+    constexpr int kHalves = Cfg::kSplitDq ? 1 : 2;  // 32-element halves of a stage per thread
     const int hr = q * 32 + lane;   // row within the half = TMEM lane
     const int r = half * 128 + hr;  // tile row
     const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16) + half * 32;
@@ -534,14 +545,15 @@ __global__ void __launch_bounds__(GemmCfg<FMT, BN, STAGE>::kThreads, 1) moe_gemm
             // each 32-element half of the stage (TMEM columns 16h .. 16h+15, column c =
             // K pair (2c, 2c+1)) is dequantised into 16 registers and stored on its own
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int hh = 0; hh < kHalves; ++hh) {
+              const int h = kHalves == 2 ? hh : kh;
               uint32_t o[16];
               if (FMT == kFmtInt4X) {  // the words of a half share its entry
-                const Int4ZpConst kc = int4zp_const(m[j][h], g.zp_float);
+                const Int4ZpConst kc = int4zp_const(h ? m[j][1] : m[j][0], g.zp_float);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                   uint32_t t4[4];
-                  int4x8_f16_zp(wd[2 * t + h], kc, t4);
+                  int4x8_f16_zp(h ? wd[2 * t + 1] : wd[2 * t], kc, t4);
 #pragma unroll
                   for (int p = 0; p < 4; ++p) o[t + 4 * p] = t4[p];
                 }
@@ -550,16 +562,16 @@ __global__ void __launch_bounds__(GemmCfg<FMT, BN, STAGE>::kThreads, 1) moe_gemm
                 for (int t = 0; t < 4; ++t) {
                   // word v = (t, h): pair p starts at k = 32h + 2t + 8p -> column 16h + t + 4p;
                   // its group scale is k / 32 (MXFP4) or k / 16 (NVFP4)
-                  const int v = 2 * t + h;
+                  const uint32_t wv = h ? wd[2 * t + 1] : wd[2 * t];
                   uint32_t t4[4];
-                  if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wd[v], m[j][0], m[j][1], t4);
-                  else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wd[v], m[j][h], m[j][h], t4);
-                  else e2m1x8_f16(wd[v], m[j][2 * h], m[j][2 * h + 1], t4);
+                  if (FMT == MOE_W_INT4_U4B8) int4x8_f16(wv, m[j][0], m[j][1], t4);
+                  else if (FMT == MOE_W_MXFP4) e2m1x8_f16(wv, h ? m[j][1] : m[j][0], h ? m[j][1] : m[j][0], t4);
+                  else e2m1x8_f16(wv, h ? m[j][2] : m[j][0], h ? m[j][3] : m[j][1], t4);
 #pragma unroll
                   for (int p = 0; p < 4; ++p) o[t + 4 * p] = t4[p];
                 }
               }
-              if (j == 0 && h == 0) {
+              if (j == 0 && hh == 0) {
                 mbar_wait(&a_empty[as], ((ak / kSA) + 1) & 1, abort_flag, g.status);
                 tc_fence_after();
               }
