@@ -552,6 +552,39 @@ __global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_sma
           if (cw == 0 && lane == 0 && u0 == 0) atomicOr(g.status, kStatusRouting);
           continue;
         }
+        // what the item's epilogue reads from global memory (scale, sorted ids,
+        // bias) is fetched before its K loop, off the critical path, where that
+        // measured faster: GEMM2 and FP4 GEMM1 up to 16-token blocks (INT4 GEMM1,
+        // which keeps per-group sums in registers, measured 1-1.5 % slower)
+        constexpr bool kEpiPf = NT <= 2 && (!kG1 || FMT == MOE_W_MXFP4 || FMT == MOE_W_NVFP4);
+        const float gsc_pf = kEpiPf ? gs_tab[e] : 0.f;
+        int sid_pf[NT][2];
+        float bias_pf[MI][2];  // gated: gate and up bias of the row; otherwise of rows h = 0, 1
+        if (kEpiPf) {
+  #pragma unroll
+          for (int n = 0; n < NT; ++n)
+  #pragma unroll
+            for (int c = 0; c < 2; ++c) sid_pf[n][c] = g.sorted_ids[b * g.block_m + n * 8 + 2 * tq + c];
+  #pragma unroll
+          for (int i = 0; i < MI; ++i) {
+            bias_pf[i][0] = 0.f;
+            bias_pf[i][1] = 0.f;
+            if (g.has_bias) {
+              if (kGated) {
+                const int f = tile * 128 + rows[i][0];
+                bias_pf[i][0] = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + f]);
+                bias_pf[i][1] = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + Npad + f]);
+              } else {
+  #pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int o = tile * 256 + rows[i][h];
+                  if (kG1) bias_pf[i][h] = bf16_bits_to_float(bias_tab[(int64_t)e * Npad + o]);
+                  else if (o < L.K) bias_pf[i][h] = bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + o]);
+                }
+              }
+            }
+          }
+        }
         float acc[MI][NT][4];
   #pragma unroll
         for (int i = 0; i < MI; ++i)
@@ -628,13 +661,16 @@ __global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_sma
                 }
           }
         }
-        const float gsc = gs_tab[e];
+        const float gsc = kEpiPf ? gsc_pf : gs_tab[e];
   #pragma unroll
         for (int i = 0; i < MI; ++i) {
           if (kGated) {
             const int f = tile * 128 + rows[i][0];
             float bg = 0.f, bu = 0.f;
-            if (g.has_bias) {
+            if (kEpiPf) {
+              bg = bias_pf[i][0];
+              bu = bias_pf[i][1];
+            } else if (g.has_bias) {
               bg = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + f]);
               bu = bf16_bits_to_float(bias_tab[(int64_t)e * 2 * Npad + Npad + f]);
             }
@@ -643,7 +679,7 @@ __global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_sma
   #pragma unroll
               for (int c = 0; c < 2; ++c) {
                 const int pos = b * g.block_m + n * 8 + 2 * tq + c;
-                const int sid = g.sorted_ids[pos];
+                const int sid = kEpiPf ? sid_pf[n][c] : g.sorted_ids[pos];
                 if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);  // neither a pair nor padding
                 const float hg = acc[i][n][c] * gsc + bg;
                 const float hu = acc[i][n][2 + c] * gsc + bu;
@@ -655,13 +691,13 @@ __global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_sma
   #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int f = tile * 256 + rows[i][h];
-              const float bf = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * Npad + f]) : 0.f;
+              const float bf = kEpiPf ? bias_pf[i][h] : (g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * Npad + f]) : 0.f);
   #pragma unroll
               for (int n = 0; n < NT; ++n)
   #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                   const int pos = b * g.block_m + n * 8 + 2 * tq + c;
-                  const int sid = g.sorted_ids[pos];
+                  const int sid = kEpiPf ? sid_pf[n][c] : g.sorted_ids[pos];
                   if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
                   const float hv = acc[i][n][2 * h + c] * gsc + bf;
                   const bool live = live_sid(sid, g.pairs);
@@ -675,13 +711,13 @@ __global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_sma
             for (int h = 0; h < 2; ++h) {
               const int o = tile * 256 + rows[i][h];
               if (o >= L.K) continue;
-              const float bo = g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + o]) : 0.f;
+              const float bo = kEpiPf ? bias_pf[i][h] : (g.has_bias ? bf16_bits_to_float(bias_tab[(int64_t)e * L.Kpad2 + o]) : 0.f);
   #pragma unroll
               for (int n = 0; n < NT; ++n)
   #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                   const int pos = b * g.block_m + n * 8 + 2 * tq + c;
-                  const int sid = g.sorted_ids[pos];
+                  const int sid = kEpiPf ? sid_pf[n][c] : g.sorted_ids[pos];
                   if ((unsigned)sid > (unsigned)g.pairs) atomicOr(g.status, kStatusRouting);
                   if (live_sid(sid, g.pairs)) {
                     const float y = acc[i][n][2 * h + c] * gsc + bo;
