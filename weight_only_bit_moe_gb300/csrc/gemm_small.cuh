@@ -646,19 +646,39 @@ __global__ void __launch_bounds__(SmallCfg<BN, STAGE>::kThreads, 1) moe_gemm_sma
             for (int n = 0; n < NT; ++n)
   #pragma unroll
               for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
-          for (int cc = c_first; cc <= c_last; ++cc) {
-            // CTA cc holds this item in its first segment iff its range starts inside the item
-            const float* src = g.partial + (int64_t)(2 * cc + (sk_lo(plan, cc) >= wu ? 0 : 1)) * kTileRows * BN;
+          // the partials of kPU CTAs are loaded before they are added (in CTA
+          // order); INT4 GEMM1, at its register limit, measured slower with it
+          constexpr bool kIntG1 = kG1 && (FMT == MOE_W_INT4_U4B8 || FMT == kFmtInt4X);
+          constexpr int kPU = kIntG1 ? 1 : (MI * NT == 1 ? 4 : (MI * NT == 2 ? 2 : 1));
+          for (int cc0 = c_first; cc0 <= c_last; cc0 += kPU) {
+            float2 pv[kPU][MI][2][NT];
   #pragma unroll
-            for (int i = 0; i < MI; ++i)
+            for (int uu = 0; uu < kPU; ++uu) {
+              const int cc = cc0 + uu;
+              if (cc > c_last) break;
+              // CTA cc holds this item in its first segment iff its range starts inside the item
+              const float* src = g.partial + (int64_t)(2 * cc + (sk_lo(plan, cc) >= wu ? 0 : 1)) * kTileRows * BN;
   #pragma unroll
-              for (int h = 0; h < 2; ++h)
+              for (int i = 0; i < MI; ++i)
   #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                  const float2 v = __ldcg(reinterpret_cast<const float2*>(src + rows[i][h] * BN + n * 8 + 2 * tq));
-                  acc[i][n][2 * h] += v.x;
-                  acc[i][n][2 * h + 1] += v.y;
-                }
+                for (int h = 0; h < 2; ++h)
+  #pragma unroll
+                  for (int n = 0; n < NT; ++n)
+                    pv[uu][i][h][n] = __ldcg(reinterpret_cast<const float2*>(src + rows[i][h] * BN + n * 8 + 2 * tq));
+            }
+  #pragma unroll
+            for (int uu = 0; uu < kPU; ++uu) {
+              if (cc0 + uu > c_last) break;
+  #pragma unroll
+              for (int i = 0; i < MI; ++i)
+  #pragma unroll
+                for (int h = 0; h < 2; ++h)
+  #pragma unroll
+                  for (int n = 0; n < NT; ++n) {
+                    acc[i][n][2 * h] += pv[uu][i][h][n].x;
+                    acc[i][n][2 * h + 1] += pv[uu][i][h][n].y;
+                  }
+            }
           }
         }
         const float gsc = kEpiPf ? gsc_pf : gs_tab[e];
