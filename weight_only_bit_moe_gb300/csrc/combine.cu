@@ -37,10 +37,13 @@ __device__ __forceinline__ void bf16x8(const uint16_t* p, float (&v)[8]) {  // 8
   }
 }
 
-// y of one pair at columns [col, col+8) (two 16-byte loads).
+// y of one pair at columns [col, col+8) (two 16-byte loads).  The loads are
+// streaming (evict-first): y is read once, and reading it with the normal
+// policy cost the int4 M=4096 combine about 54 us of its 122 (the lines it
+// allocated pushed GEMM2's dirty y lines and each other out of L2).
 __device__ __forceinline__ void pair_y8(const CombineArgs& c, int pair, int col, float (&v)[8]) {
   const float4* p = reinterpret_cast<const float4*>(c.y + (int64_t)pair * c.K + col);
-  const float4 a = __ldcg(p), b = __ldcg(p + 1);
+  const float4 a = __ldcs(p), b = __ldcs(p + 1);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
