@@ -38,9 +38,9 @@ __device__ __forceinline__ void bf16x8(const uint16_t* p, float (&v)[8]) {  // 8
 }
 
 // y of one pair at columns [col, col+8) (two 16-byte loads).  The loads are
-// streaming (evict-first): y is read once, and reading it with the normal
-// policy cost the int4 M=4096 combine about 54 us of its 122 (the lines it
-// allocated pushed GEMM2's dirty y lines and each other out of L2).
+// streaming (evict-first): y is read once, and the normal policy measured about
+// 54 us slower on the int4 M=4096 combine (122 us).  Storing y with streaming
+// stores in GEMM2 as well measured no different.
 __device__ __forceinline__ void pair_y8(const CombineArgs& c, int pair, int col, float (&v)[8]) {
   const float4* p = reinterpret_cast<const float4*>(c.y + (int64_t)pair * c.K + col);
   const float4 a = __ldcs(p), b = __ldcs(p + 1);
