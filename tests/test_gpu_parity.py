@@ -98,7 +98,8 @@ def test_forward_small(name):
     assert layer.status() == 0
 
 
-@pytest.mark.parametrize("name", ["int4-zipf-small", "int4-relu2-small", "nvfp4-ep-small", "mxfp4-alpha-small"])
+@pytest.mark.parametrize("name", ["int4-zipf-small", "int4-relu2-small", "nvfp4-ep-small", "mxfp4-alpha-small",
+                                  "mxfp4-relu2-small"])
 @pytest.mark.parametrize("B", [8, 16, 32, 64, 128])
 def test_forward_every_block_m(name, B):
     wl = GPU_SMALL[name]
