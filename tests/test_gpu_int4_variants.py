@@ -45,7 +45,7 @@ VARIANTS = {
 
 
 @pytest.mark.parametrize("name", sorted(VARIANTS))
-@pytest.mark.parametrize("block_m", [8, 16, 64, 128])
+@pytest.mark.parametrize("block_m", [8, 16, 32, 64, 128])
 def test_int4_variant_parity(name, block_m):
     from weight_only_bit_moe_gb300 import binding as B
     from weight_only_bit_moe_gb300.layer import MoELayer
